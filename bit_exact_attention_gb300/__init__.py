@@ -1,1 +1,201 @@
-"""GB300-native SageAttention2 quantized attention forward (placeholder; binding added below)."""
+"""GB300-native SageAttention2 quantized exact-attention forward.
+
+Thin Python binding over the C ABI in ``include/sage2_attn.h`` (library
+``libsage2_attn.so``, built in-tree for sm_103a). The functions here only check
+and marshal arguments -- torch tensors give device pointers and the current
+stream -- and every step of the computation runs in the library's kernels. There
+is no CPU path: without the built library (or without an sm_103 GPU) every call
+raises.
+
+Shapes follow the library: dense ``q [B, Nq, Hq, D]``, ``k, v [B, Nkv, Hkv, D]``;
+varlen packed ``[total, H, D]`` with int32 ``cu_seqlens`` on the device.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import BF16, FP16, FP32, Sage2Error, WsLayout  # noqa: F401
+
+__all__ = ["attn_fwd", "attn_fwd_varlen", "prepass", "attention", "prepass_varlen",
+           "attention_varlen", "workspace_size", "workspace_layout", "device_status",
+           "alloc_workspace", "debug_tile", "debug_timeout", "Sage2Error", "load_library"]
+
+_DT = {torch.float16: FP16, torch.bfloat16: BF16, torch.float32: FP32}
+
+
+def load_library():
+    """Loads (building first if needed) and returns the ctypes library handle."""
+    return _lib.lib()
+
+
+def _code(dtype: torch.dtype) -> int:
+    if dtype not in _DT:
+        raise TypeError(f"unsupported dtype {dtype}")
+    return _DT[dtype]
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q=None, total_kv=None) -> int:
+    total_q = B * max_nq if total_q is None else total_q
+    total_kv = B * max_nkv if total_kv is None else total_kv
+    n = _lib.lib().sage2_workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv)
+    if n == 0:
+        raise Sage2Error(_lib.EINVAL, "sage2_workspace_size")
+    return int(n)
+
+
+def workspace_layout(B, Hq, Hkv, max_nq, max_nkv, D, total_q=None, total_kv=None) -> WsLayout:
+    total_q = B * max_nq if total_q is None else total_q
+    total_kv = B * max_nkv if total_kv is None else total_kv
+    L = WsLayout()
+    _lib.check(_lib.lib().sage2_workspace_layout(B, Hq, Hkv, max_nq, max_nkv, D, total_q,
+                                                 total_kv, ctypes.byref(L)),
+               "sage2_workspace_layout")
+    return L
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(workspace, nbytes, device):
+    if workspace is None:
+        workspace = alloc_workspace(nbytes, device)
+    _dev(workspace, "workspace")
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise Sage2Error(_lib.EWORKSPACE, "workspace")
+    return workspace
+
+
+def _out(out, shape, dtype, device):
+    if out is None:
+        out = torch.empty(shape, dtype=dtype, device=device)
+    _dev(out, "out")
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out has shape {tuple(out.shape)}, expected {tuple(shape)}")
+    return out
+
+
+def attn_fwd(q, k, v, causal=False, sm_scale=0.0, out=None, out_dtype=None, workspace=None,
+             stream=None):
+    """softmax(Q K^T * sm_scale) V the SageAttention2 way; q [B, Nq, Hq, D], k/v [B, Nkv, Hkv, D]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t, n)
+    B, Nq, Hq, D = q.shape
+    _, Nkv, Hkv, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes/dtypes disagree")
+    odt = q.dtype if out_dtype is None else out_dtype
+    out = _out(out, (B, Nq, Hq, D), odt, q.device)
+    ws = _ws(workspace, workspace_size(B, Hq, Hkv, Nq, Nkv, D), q.device)
+    _lib.check(_lib.lib().sage2_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _code(q.dtype), _code(out.dtype), B, Hq, Hkv, Nq,
+        Nkv, D, int(bool(causal)), float(sm_scale), _ptr(ws), ws.numel(), _stream(stream)),
+        "sage2_attn_fwd")
+    return out
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, causal=False,
+                    sm_scale=0.0, out=None, out_dtype=None, workspace=None, stream=None):
+    """Packed variable-length form: q [total_q, Hq, D], k/v [total_kv, Hkv, D], cu_seqlens int32 (B+1)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cu_seqlens_q, "cu_seqlens_q"),
+                 (cu_seqlens_kv, "cu_seqlens_kv")):
+        _dev(t, n)
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_kv.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    total_q, Hq, D = q.shape
+    total_kv, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    odt = q.dtype if out_dtype is None else out_dtype
+    out = _out(out, (total_q, Hq, D), odt, q.device)
+    ws = _ws(workspace, workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv), q.device)
+    _lib.check(_lib.lib().sage2_attn_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _code(q.dtype), _code(out.dtype),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq, Hkv, max_nq, max_nkv, total_q, total_kv,
+        D, int(bool(causal)), float(sm_scale), _ptr(ws), ws.numel(), _stream(stream)),
+        "sage2_attn_fwd_varlen")
+    return out
+
+
+def prepass(q, k, v, workspace, causal=False, sm_scale=0.0, stream=None):
+    B, Nq, Hq, D = q.shape
+    _, Nkv, Hkv, _ = k.shape
+    _lib.check(_lib.lib().sage2_prepass(
+        _ptr(q), _ptr(k), _ptr(v), _code(q.dtype), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)),
+        float(sm_scale), _ptr(workspace), workspace.numel(), _stream(stream)), "sage2_prepass")
+
+
+def attention(out, workspace, B, Hq, Hkv, Nq, Nkv, D, causal=False, sm_scale=0.0, stream=None):
+    _lib.check(_lib.lib().sage2_attention(
+        _ptr(out), _code(out.dtype), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), float(sm_scale),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "sage2_attention")
+
+
+def prepass_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, workspace,
+                   causal=False, sm_scale=0.0, stream=None):
+    total_q, Hq, D = q.shape
+    total_kv, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    _lib.check(_lib.lib().sage2_prepass_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _code(q.dtype), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq,
+        Hkv, max_nq, max_nkv, total_q, total_kv, D, int(bool(causal)), float(sm_scale),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "sage2_prepass_varlen")
+
+
+def attention_varlen(out, workspace, cu_seqlens_q, cu_seqlens_kv, Hkv, max_nq, max_nkv,
+                     total_kv, causal=False, sm_scale=0.0, stream=None):
+    total_q, Hq, D = out.shape
+    B = cu_seqlens_q.numel() - 1
+    _lib.check(_lib.lib().sage2_attention_varlen(
+        _ptr(out), _code(out.dtype), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq, Hkv, max_nq,
+        max_nkv, total_q, total_kv, D, int(bool(causal)), float(sm_scale), _ptr(workspace),
+        workspace.numel(), _stream(stream)), "sage2_attention_varlen")
+
+
+def device_status(workspace, stream=None) -> tuple[int, int]:
+    """(status code, raw status word) after synchronizing the stream."""
+    raw = ctypes.c_int(0)
+    rc = _lib.lib().sage2_device_status(_ptr(workspace), _stream(stream), ctypes.byref(raw))
+    return int(rc), int(raw.value)
+
+
+def debug_tile(workspace, B, Hq, Hkv, max_nq, max_nkv, D, causal, b, h, qt, kt, sm_scale=0.0,
+               cu_seqlens_q=None, cu_seqlens_kv=None, total_q=None, total_kv=None, stream=None):
+    """Raw (S accumulators, P~ bytes, fresh P~V partial) of one KV tile of one work unit."""
+    dev = workspace.device
+    Dp = 64 if D <= 64 else 128
+    s_out = torch.zeros(128, 128, dtype=torch.float32, device=dev)
+    p_out = torch.zeros(128, 128, dtype=torch.uint8, device=dev)
+    r_out = torch.zeros(128, Dp, dtype=torch.float32, device=dev)
+    total_q = B * max_nq if total_q is None else total_q
+    total_kv = B * max_nkv if total_kv is None else total_kv
+    _lib.check(_lib.lib().sage2_debug_tile(
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq, Hkv, max_nq, max_nkv, total_q, total_kv,
+        D, int(bool(causal)), float(sm_scale), _ptr(workspace), workspace.numel(), b, h, qt, kt,
+        _ptr(s_out), _ptr(p_out), _ptr(r_out), _stream(stream)), "sage2_debug_tile")
+    return s_out, p_out, r_out
+
+
+def debug_timeout(workspace, B, Hq, Hkv, Nq, Nkv, D, stream=None):
+    _lib.check(_lib.lib().sage2_debug_timeout(B, Hq, Hkv, Nq, Nkv, D, _ptr(workspace),
+                                              workspace.numel(), _stream(stream)),
+               "sage2_debug_timeout")

@@ -1,0 +1,159 @@
+/*
+ * sage2_attn.h -- C ABI of the GB300 (sm_103a) SageAttention2 quantized attention forward.
+ *
+ * What it computes: exact attention O = softmax(Q K^T * sm_scale) V, evaluated the
+ * SageAttention2 way (sources: the web pages "SageAttention2 and Fast Exact INT4
+ * Attention" visual companion, sections Visual Thesis, Numerical Repair Stack and
+ * Per-Thread INT4 Geometry; "SageAttention2: Efficient Attention with Thorough Outlier
+ * Smoothing and Per-thread INT4 Quantization" research note, its three components;
+ * PMLR v267 zhang25ae, Abstract):
+ *   1. K is smoothed by its per-(sequence, kv head) channel mean; Q by the mean of each
+ *      block of 128 rows, with the correction DeltaS = qmean . (K - kmean)^T added back
+ *      to the logits.
+ *   2. Smoothed Q and K are put on the INT4 grid [-7, 7]: one FP32 scale per Q row and
+ *      one per 32 consecutive K tokens (the thread-owned groups of the tensor-memory
+ *      accumulator layout). Q K^T of the codes is exact (integer valued).
+ *   3. V is quantized per channel to FP8 e4m3 (scale amax/448); P~ = e4m3(448 P).
+ *   4. P~ V is accumulated per 128-key block into a fresh FP32 partial in tensor memory,
+ *      then folded into an FP32 accumulator on the CUDA cores (two-level accumulation).
+ * Interface envelope (visual companion, Per-Thread INT4 Geometry, implementation panel):
+ * GQA, different q and kv lengths, packed variable-length batches, head dim padded to
+ * 64 or 128, head dims above 128 rejected.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are token-major: dense calls take q [B, Nq, Hq, D], k and v [B, Nkv, Hkv, D],
+ *     out [B, Nq, Hq, D]; varlen calls take the packed forms [total, H, D] with
+ *     cu_seqlens (int32, B + 1 prefix sums). All row-major and contiguous.
+ *   - q, k, v, out, workspace are DEVICE pointers owned by the caller; nothing is retained
+ *     after a call returns. Pointers must be 16-byte aligned; the workspace 1024-byte aligned.
+ *   - in_dtype: SAGE2_FP16 or SAGE2_BF16. out_dtype: the input dtype or SAGE2_FP32.
+ *   - D (the head dim of the tensors, called D0 in the comments) must satisfy 8 <= D <= 128
+ *     and D % 8 == 0; it is computed as 64 (D <= 64) or 128 (D <= 128) with zero channels.
+ *   - Hq % Hkv == 0 (GQA: q head h reads kv head h / (Hq / Hkv)).
+ *   - causal: key j is visible to query i of a sequence iff j <= i + Nkv - Nq (aligned at
+ *     the bottom-right); a row with no visible key outputs 0.
+ *   - sm_scale <= 0 selects 1/sqrt(D).
+ *   - stream is a cudaStream_t (NULL = legacy default stream). Calls are asynchronous on it:
+ *     the return code covers argument checks and launch errors only; a device-side wait
+ *     that gave up is reported later by sage2_device_status().
+ *   - Two calls that share a workspace must be ordered (same stream, or synchronized).
+ *   - The device must be sm_103 (GB300); other devices return SAGE2_EUNSUPPORTED.
+ */
+#ifndef SAGE2_ATTN_H
+#define SAGE2_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SAGE2_OK = 0,
+  SAGE2_EINVAL = -1,          /* bad argument: null/misaligned pointer, bad size, Hq % Hkv */
+  SAGE2_EUNSUPPORTED = -2,    /* head dim > 128 or not a multiple of 8, or not an sm_103 GPU */
+  SAGE2_EWORKSPACE = -3,      /* workspace smaller than sage2_workspace_size() or misaligned */
+  SAGE2_ECUDA = -4,           /* a CUDA call (launch, copy, tensor-map encode) failed */
+  SAGE2_EDEVICE_TIMEOUT = -5  /* a bounded device-side wait expired (kernel returned early) */
+} sage2_status;
+
+typedef enum { SAGE2_FP16 = 0, SAGE2_BF16 = 1, SAGE2_FP32 = 2 } sage2_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *sage2_status_str(int status);
+
+/* Library ABI version: 100 * major + minor. */
+int sage2_version(void);
+
+/* Bytes of device workspace a call with these sizes needs (0 on invalid sizes).
+ * Dense calls: total_q = B * Nq, total_kv = B * Nkv, max_Nq = Nq, max_Nkv = Nkv. */
+size_t sage2_workspace_size(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D, int total_q,
+                            int total_kv);
+
+/* Full forward (prepass + attention) on dense [B, N, H, D] tensors. */
+int sage2_attn_fwd(const void *q, const void *k, const void *v, void *out, int in_dtype,
+                   int out_dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal,
+                   float sm_scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Full forward on packed variable-length batches. cu_seqlens_q / cu_seqlens_kv are
+ * DEVICE int32 arrays of B + 1 prefix sums whose last entries equal total_q / total_kv;
+ * max_Nq / max_Nkv bound every sequence length (checked on the device: a sequence that
+ * exceeds them is skipped and reported through sage2_device_status). */
+int sage2_attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, int in_dtype,
+                          int out_dtype, const int *cu_seqlens_q, const int *cu_seqlens_kv, int B,
+                          int Hq, int Hkv, int max_Nq, int max_Nkv, int total_q, int total_kv,
+                          int D, int causal, float sm_scale, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/* The two halves of the forward, for callers (and benchmarks) that time or schedule them
+ * apart. sage2_prepass*: smoothing and quantization only (K/V statistics, Q/K INT4 codes
+ * and scales, V e4m3 codes transposed, DeltaS), written into the workspace.
+ * sage2_attention*: the fused attention kernel only, reading a workspace that a prepass
+ * call with the same arguments filled. */
+int sage2_prepass(const void *q, const void *k, const void *v, int in_dtype, int B, int Hq,
+                  int Hkv, int Nq, int Nkv, int D, int causal, float sm_scale, void *workspace,
+                  size_t workspace_bytes, void *stream);
+int sage2_attention(void *out, int out_dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                    int causal, float sm_scale, const void *workspace, size_t workspace_bytes,
+                    void *stream);
+int sage2_prepass_varlen(const void *q, const void *k, const void *v, int in_dtype,
+                         const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq,
+                         int Hkv, int max_Nq, int max_Nkv, int total_q, int total_kv, int D,
+                         int causal, float sm_scale, void *workspace, size_t workspace_bytes,
+                         void *stream);
+int sage2_attention_varlen(void *out, int out_dtype, const int *cu_seqlens_q,
+                           const int *cu_seqlens_kv, int B, int Hq, int Hkv, int max_Nq,
+                           int max_Nkv, int total_q, int total_kv, int D, int causal,
+                           float sm_scale, const void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* Synchronizes `stream`, then reads the workspace's device status word (cleared by every
+ * prepass). Returns SAGE2_OK, SAGE2_EDEVICE_TIMEOUT (a bounded wait expired) or
+ * SAGE2_EINVAL (a varlen sequence exceeded max_Nq/max_Nkv); *raw (if not NULL) receives
+ * the word itself (0 when clean; otherwise a code naming the wait that gave up). */
+int sage2_device_status(const void *workspace, void *stream, int *raw);
+
+/* Byte offsets of the buffers inside a workspace, for tests and tools that read the
+ * intermediate results. Layouts (Tq, Tkv = padded token counts; every sequence starts on a
+ * 128-row boundary at row 128 * (cu_seqlens[b] / 128 + b)):
+ *   qcode  u8 (e4m3 bytes holding integers in [-7,7]) [Hq][Tq][Dp]
+ *   kcode  u8 (same)                                  [Hkv][Tkv][Dp]
+ *   vcodeT u8 (e4m3)                                  [Hkv][Dp][Tkv]
+ *   qscale f32 [Hq][Tq]        kscale f32 [Hkv][Tkv/32]
+ *   qmean  f32 [Hq][Tq/128][Dp]
+ *   kmean  f32 [B][Hkv][Dp]    vscale f32 [B][Hkv][Dp] (amax/448)
+ *   dsc    f32 [Hq][Tq/128][Nkv_pad] = fl32(DeltaS * log2(e) * sm_scale) */
+typedef struct {
+  size_t total_bytes;
+  size_t qcode, kcode, vcodeT, qscale, kscale, qmean, kmean, vscale, vinv, dsc;
+  size_t kpart, vpart, status;
+  int Dp, Tq, Tkv, nkv_pad, nchunk;
+} sage2_ws_layout;
+
+int sage2_workspace_layout(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D, int total_q,
+                           int total_kv, sage2_ws_layout *layout);
+
+/* Test hook (unstable): reruns the attention kernel for the single (sequence b, q head h,
+ * q tile qt) work unit on a prepared workspace and dumps, for its KV tile kt, the raw
+ * integer Q K^T accumulators (s_out: f32 [128][128], exact integers), the P~ e4m3 bytes
+ * (p_out: u8 [128][128]) and the fresh P~V partial (r_out: f32 [128][Dp]), all device
+ * buffers. Same size arguments as sage2_attention_varlen (cu_seqlens may be NULL for dense
+ * inputs, then Nq = max_Nq and Nkv = max_Nkv for every sequence). */
+int sage2_debug_tile(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq, int Hkv,
+                     int max_Nq, int max_Nkv, int total_q, int total_kv, int D, int causal,
+                     float sm_scale, const void *workspace, size_t workspace_bytes, int b, int h,
+                     int qt, int kt, float *s_out, uint8_t *p_out, float *r_out, void *stream);
+
+/* Test hook (unstable): runs one attention work unit whose producer never issues its
+ * loads, so every consumer wait must expire (about one second); the kernel must return on
+ * its own and leave SAGE2_EDEVICE_TIMEOUT in the workspace status word. Needs a workspace
+ * filled by a prepass with the same sizes. */
+int sage2_debug_timeout(int B, int Hq, int Hkv, int Nq, int Nkv, int D, const void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE2_ATTN_H */

@@ -1,0 +1,164 @@
+"""Helpers for the GPU parity tests: run the library, read its workspace back in the
+oracle's layouts, run the oracle on the same seeded inputs, compare.
+
+The oracle only ever sees the seeded inputs; nothing computed by the CUDA path is fed
+to it.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import bit_exact_attention_gb300 as S
+from bit_exact_attention_gb300 import workloads as W
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def pad_starts(cu):
+    return [128 * (cu[b] // 128 + b) for b in range(len(cu) - 1)]
+
+
+def metrics(a: np.ndarray, r: np.ndarray) -> dict:
+    a = np.asarray(a, np.float64).ravel()
+    r = np.asarray(r, np.float64).ravel()
+    den = np.abs(r).sum()
+    cos = float(a @ r / math.sqrt((a @ a) * (r @ r))) if (a @ a) > 0 and (r @ r) > 0 else float(
+        np.array_equal(a, r))
+    return {"relL1": float(np.abs(a - r).sum() / den) if den > 0 else float(np.abs(a - r).sum()),
+            "maxabs": float(np.abs(a - r).max()) if a.size else 0.0, "cos": cos}
+
+
+def e4m3_to_int(u8: torch.Tensor) -> np.ndarray:
+    return u8.contiguous().view(torch.float8_e4m3fn).to(torch.float32).cpu().numpy().astype(np.int64)
+
+
+def e4m3_to_f64(u8: torch.Tensor) -> np.ndarray:
+    return u8.contiguous().view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy()
+
+
+class GpuRun:
+    """Inputs on the GPU plus a workspace; prepass / attention / debug hooks."""
+
+    def __init__(self, w: W.Workload, x: dict, causal=None, sm_scale=0.0):
+        self.w, self.x = w, x
+        self.causal = w.causal if causal is None else causal
+        self.sm_scale = sm_scale
+        self.B = w.batch
+        self.max_nq, self.max_nkv = max(w.nq), max(w.nkv)
+        self.tq, self.tkv = sum(w.nq), sum(w.nkv)
+        self.q = x["q"].cuda()
+        self.k = x["k"].cuda()
+        self.v = x["v"].cuda()
+        self.cu_q = torch.tensor(x["cu_q"], dtype=torch.int32, device="cuda")
+        self.cu_kv = torch.tensor(x["cu_kv"], dtype=torch.int32, device="cuda")
+        self.L = S.workspace_layout(self.B, w.hq, w.hkv, self.max_nq, self.max_nkv, w.d,
+                                    self.tq, self.tkv)
+        self.ws = S.alloc_workspace(self.L.total_bytes)
+        self.off0 = (-self.ws.data_ptr()) % 1024
+
+    def prepass(self):
+        S.prepass_varlen(self.q, self.k, self.v, self.cu_q, self.cu_kv, self.max_nq,
+                         self.max_nkv, self.ws, causal=self.causal, sm_scale=self.sm_scale)
+
+    def attention(self, out_dtype=torch.float32):
+        out = torch.empty(self.tq, self.w.hq, self.w.d, dtype=out_dtype, device="cuda")
+        S.attention_varlen(out, self.ws, self.cu_q, self.cu_kv, self.w.hkv, self.max_nq,
+                           self.max_nkv, self.tkv, causal=self.causal, sm_scale=self.sm_scale)
+        return out
+
+    def forward(self, out_dtype=None):
+        return S.attn_fwd_varlen(self.q, self.k, self.v, self.cu_q, self.cu_kv, self.max_nq,
+                                 self.max_nkv, causal=self.causal, sm_scale=self.sm_scale,
+                                 out_dtype=out_dtype, workspace=self.ws)
+
+    def status(self):
+        return S.device_status(self.ws)
+
+    def debug_tile(self, b, h, qt, kt):
+        return S.debug_tile(self.ws, self.B, self.w.hq, self.w.hkv, self.max_nq, self.max_nkv,
+                            self.w.d, self.causal, b, h, qt, kt, sm_scale=self.sm_scale,
+                            cu_seqlens_q=self.cu_q, cu_seqlens_kv=self.cu_kv, total_q=self.tq,
+                            total_kv=self.tkv)
+
+    # ---------------------------------------------------------------- workspace views
+    def _buf(self, off, count, dtype):
+        nbytes = count * torch.tensor([], dtype=dtype).element_size()
+        return self.ws[self.off0 + off: self.off0 + off + nbytes].view(dtype)
+
+    def views(self):
+        L, w = self.L, self.w
+        Dp = L.Dp
+        return {
+            "qcode": self._buf(L.qcode, w.hq * L.Tq * Dp, torch.uint8).view(w.hq, L.Tq, Dp),
+            "kcode": self._buf(L.kcode, w.hkv * L.Tkv * Dp, torch.uint8).view(w.hkv, L.Tkv, Dp),
+            "vcodeT": self._buf(L.vcodeT, w.hkv * Dp * L.Tkv, torch.uint8).view(w.hkv, Dp, L.Tkv),
+            "qscale": self._buf(L.qscale, w.hq * L.Tq, torch.float32).view(w.hq, L.Tq),
+            "kscale": self._buf(L.kscale, w.hkv * L.Tkv // 32, torch.float32).view(w.hkv, L.Tkv // 32),
+            "qmean": self._buf(L.qmean, w.hq * (L.Tq // 128) * Dp, torch.float32).view(w.hq, L.Tq // 128, Dp),
+            "kmean": self._buf(L.kmean, self.B * w.hkv * Dp, torch.float32).view(self.B, w.hkv, Dp),
+            "vscale": self._buf(L.vscale, self.B * w.hkv * Dp, torch.float32).view(self.B, w.hkv, Dp),
+            "dsc": self._buf(L.dsc, w.hq * (L.Tq // 128) * L.nkv_pad, torch.float32).view(
+                w.hq, L.Tq // 128, L.nkv_pad),
+        }
+
+    def gathered(self):
+        """The prepass results in the oracle's (token-major, unpadded) layouts."""
+        v = {k: t.cpu() for k, t in self.views().items()}
+        w, x = self.w, self.x
+        qp, kp = pad_starts(x["cu_q"]), pad_starts(x["cu_kv"])
+        Dp = self.L.Dp
+        qc = np.zeros((self.tq, w.hq, Dp), np.int64)
+        sq = np.zeros((self.tq, w.hq), np.float32)
+        kc = np.zeros((self.tkv, w.hkv, Dp), np.int64)
+        sk = np.zeros((self.tkv, w.hkv), np.float32)
+        vc = np.zeros((self.tkv, w.hkv, Dp), np.float64)
+        for b in range(self.B):
+            q0, nq = x["cu_q"][b], w.nq[b]
+            k0, nkv = x["cu_kv"][b], w.nkv[b]
+            qc[q0:q0 + nq] = e4m3_to_int(v["qcode"][:, qp[b]:qp[b] + nq]).transpose(1, 0, 2)
+            sq[q0:q0 + nq] = v["qscale"][:, qp[b]:qp[b] + nq].numpy().T
+            kc[k0:k0 + nkv] = e4m3_to_int(v["kcode"][:, kp[b]:kp[b] + nkv]).transpose(1, 0, 2)
+            toks = np.arange(nkv)
+            sk[k0:k0 + nkv] = v["kscale"][:, (kp[b] + toks) // 32].numpy().T
+            vc[k0:k0 + nkv] = e4m3_to_f64(v["vcodeT"][:, :, kp[b]:kp[b] + nkv]).transpose(2, 0, 1)
+        return {"qcode": qc, "qscale": sq, "kcode": kc, "kscale": sk, "vcode": vc,
+                "kmean": v["kmean"].numpy(), "vscale": v["vscale"].numpy(),
+                "qmean": v["qmean"].numpy(), "dsc": v["dsc"].numpy(), "raw": v}
+
+
+def units_sample(w: W.Workload, n: int, seed: int = 0):
+    """>= n (b, h, q-block) units: always the last (possibly partial) block of each sequence,
+    the first block, a causal-diagonal block, then seeded random ones."""
+    rng = np.random.default_rng(seed)
+    units = set()
+    for b in range(w.batch):
+        nqb = (w.nq[b] + 127) // 128
+        if nqb == 0:
+            continue
+        for h in sorted({0, w.hq - 1}):
+            units.add((b, h, nqb - 1))
+            units.add((b, h, 0))
+            units.add((b, h, nqb // 2))
+    while len(units) < n:
+        b = int(rng.integers(w.batch))
+        nqb = (w.nq[b] + 127) // 128
+        if nqb == 0:
+            continue
+        units.add((b, int(rng.integers(w.hq)), int(rng.integers(nqb))))
+    return sorted(units)
+
+
+def unit_rows(w: W.Workload, cu_q, units):
+    """Index arrays (token, head) of the rows the units cover."""
+    toks, heads = [], []
+    for b, h, qb in units:
+        r0, r1 = qb * 128, min(w.nq[b], qb * 128 + 128)
+        t = np.arange(cu_q[b] + r0, cu_q[b] + r1)
+        toks.append(t)
+        heads.append(np.full_like(t, h))
+    return np.concatenate(toks), np.concatenate(heads)

@@ -1,0 +1,294 @@
+"""GPU parity: the CUDA path against the CPU oracle, through the C ABI.
+
+Gates (per the method's emulation, the oracle's Mode Q):
+  * prepass results (means, INT4 codes and scales, e4m3 V codes, DeltaS*c) bit-exact;
+  * the raw integer Q K^T accumulators of the tensor-core MMA bit-exact;
+  * the output (FP32) within relative L1 1e-3 and max abs 2e-3;
+  * fp16/bf16 outputs within one unit in the last place of the oracle's rounded output.
+Against exact FP64 attention (Mode E) the GPU must be as accurate as the emulation itself.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bit_exact_attention_gb300 as S
+from bit_exact_attention_gb300 import workloads as W
+from parity_util import GpuRun, bits, e4m3_to_f64, metrics, pad_starts, unit_rows, units_sample
+
+pytestmark = pytest.mark.gpu
+
+REL_L1, MAX_ABS = 1e-3, 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    major, minor = torch.cuda.get_device_capability()
+    assert (major, minor) == (10, 3), f"expected an sm_103 GPU, got sm_{major}{minor}"
+    oracle.build()
+    S.load_library()
+
+
+def c32_of(w, sm_scale=0.0):
+    s = np.float32(sm_scale) if sm_scale > 0 else np.float32(1.0 / math.sqrt(w.d))
+    return np.float32(1.4426950408889634 * float(s))
+
+
+# Scaled workloads: the oracle finishes each in seconds; each spans several tiles and a
+# ragged tail.
+SCALED = {
+    "tiny": W.TINY,
+    "prefill": W.scaled(W.PREFILL, (700, 300), (700, 300), hq=4, hkv=4, name="prefill_s"),
+    "gqa": W.scaled(W.GQA_LONG, (1000,), (1000,), hq=8, hkv=2, name="gqa_s"),
+    "dit": W.scaled(W.VIDEO_DIT, (600, 333), (600, 333), hq=3, hkv=3, name="dit_s"),
+    "varlen": W.scaled(W.VARLEN, (300, 77, 129), (500, 129, 1000), hq=8, hkv=2, name="varlen_s"),
+}
+
+
+def oracle_ref(w, x, units=None, mode="emu", **kw):
+    args = (bits(x["q"]), bits(x["k"]), bits(x["v"]), W.dtype_code(w), x["cu_q"], x["cu_kv"],
+            w.hq, w.hkv, w.d, w.causal)
+    if mode == "emu":
+        return oracle.attention_emulated(*args, units=units, **kw)
+    return oracle.attention_exact(*args, units=units)
+
+
+_cache = {}
+
+
+def run_case(name):
+    if name not in _cache:
+        w = SCALED[name]
+        x = W.make_inputs(w)
+        g = GpuRun(w, x)
+        _cache[name] = (w, x, g)
+    return _cache[name]
+
+
+# ------------------------------------------------------------------ prepass
+@pytest.mark.parametrize("name", list(SCALED))
+def test_prepass_bit_exact(name):
+    w, x, g = run_case(name)
+    g.prepass()
+    assert g.status() == (0, 0)
+    got = g.gathered()
+    dt = W.dtype_code(w)
+    kmean, vamax = oracle.kv_stats(bits(x["k"]), bits(x["v"]), dt, x["cu_kv"], w.hkv, w.d)
+    qmean, qc, sq = oracle.quant_q(bits(x["q"]), dt, x["cu_q"], w.hq, w.d)
+    kc, sk = oracle.quant_k(bits(x["k"]), dt, x["cu_kv"], w.hkv, w.d, kmean=kmean)
+    vc, sv = oracle.quant_v(bits(x["v"]), dt, x["cu_kv"], w.hkv, w.d, vamax)
+    np.testing.assert_array_equal(got["kmean"], kmean)
+    np.testing.assert_array_equal(got["vscale"], sv)
+    assert int((got["qcode"] != qc).sum()) == 0, "Q code mismatches"
+    np.testing.assert_array_equal(got["qscale"], sq)
+    assert int((got["kcode"] != kc).sum()) == 0, "K code mismatches"
+    np.testing.assert_array_equal(got["kscale"], sk)
+    np.testing.assert_array_equal(got["vcode"], oracle.e4m3_decode(vc))
+    # Q block means and DeltaS * c for every (q head, Q block, visited KV tile)
+    qp, kp = pad_starts(x["cu_q"]), pad_starts(x["cu_kv"])
+    c32 = c32_of(w)
+    from bit_exact_attention_gb300 import workloads as _  # noqa: F401
+    for b in range(w.batch):
+        nqb = (w.nq[b] + 127) // 128
+        for h in range(w.hq):
+            for qb in range(nqb):
+                blk = qp[b] // 128 + qb
+                np.testing.assert_array_equal(got["qmean"][h, blk], qmean[b, h, qb])
+                ds = oracle.delta_s(bits(x["k"]), dt, x["cu_kv"], b, w.hkv, h // (w.hq // w.hkv),
+                                    w.d, kmean, qmean[b, h, qb])
+                ntiles = _kv_tiles(qb, w.nq[b], w.nkv[b], w.causal)
+                n = min(w.nkv[b], ntiles * 128)
+                want = (ds[:n] * c32).astype(np.float32)
+                np.testing.assert_array_equal(got["dsc"][h, blk, :n], want, err_msg=f"{b},{h},{qb}")
+
+
+def _kv_tiles(qt, nq, nkv, causal):
+    nt = (nkv + 127) // 128
+    if not causal:
+        return nt
+    i_last = min(qt * 128 + 127, nq - 1)
+    j_max = i_last + (nkv - nq)
+    return 0 if j_max < 0 else min(nt, j_max // 128 + 1)
+
+
+# ------------------------------------------------------------------ integer accumulators
+@pytest.mark.parametrize("name", ["tiny", "prefill", "dit", "varlen"])
+def test_qk_accumulators_bit_exact_and_pv_partial(name):
+    w, x, g = run_case(name)
+    g.prepass()
+    dt = W.dtype_code(w)
+    kmean, vamax = oracle.kv_stats(bits(x["k"]), bits(x["v"]), dt, x["cu_kv"], w.hkv, w.d)
+    _, qc, _ = oracle.quant_q(bits(x["q"]), dt, x["cu_q"], w.hq, w.d)
+    kc, _ = oracle.quant_k(bits(x["k"]), dt, x["cu_kv"], w.hkv, w.d, kmean=kmean)
+    vc, _ = oracle.quant_v(bits(x["v"]), dt, x["cu_kv"], w.hkv, w.d, vamax)
+    vval = oracle.e4m3_decode(vc)
+    Dp = g.L.Dp
+    checked = 0
+    for b in range(w.batch):
+        nqb = (w.nq[b] + 127) // 128
+        for (h, qt) in {(0, 0), (w.hq - 1, nqb - 1), (w.hq // 2, nqb // 2)}:
+            if nqb == 0:
+                continue
+            T = _kv_tiles(qt, w.nq[b], w.nkv[b], w.causal)
+            for kt in sorted({0, T - 1}):
+                if kt < 0:
+                    continue
+                s_out, p_out, r_out = g.debug_tile(b, h, qt, kt)
+                A = np.zeros((128, Dp), np.int64)
+                rows = np.arange(qt * 128, min(w.nq[b], qt * 128 + 128))
+                A[: len(rows)] = qc[x["cu_q"][b] + rows, h]
+                Kt = np.zeros((128, Dp), np.int64)
+                keys = np.arange(kt * 128, min(w.nkv[b], kt * 128 + 128))
+                hk = h // (w.hq // w.hkv)
+                Kt[: len(keys)] = kc[x["cu_kv"][b] + keys, hk]
+                want = A @ Kt.T
+                got = s_out.cpu().numpy()
+                assert np.array_equal(got, want.astype(np.float64)), (
+                    f"{name} b{b} h{h} qt{qt} kt{kt}: {(got != want).sum()} accumulator mismatches")
+                # the fresh P~V partial: P~ bytes as dumped, V codes from the oracle, FP64
+                Vt = np.zeros((128, Dp))
+                Vt[: len(keys)] = vval[x["cu_kv"][b] + keys, hk]
+                R_ref = e4m3_to_f64(p_out) @ Vt
+                R = r_out.cpu().numpy()
+                np.testing.assert_allclose(R, R_ref, rtol=1e-5, atol=1e-3 * np.abs(R_ref).max())
+                checked += 1
+    assert checked >= 2
+
+
+# ------------------------------------------------------------------ outputs
+@pytest.mark.parametrize("name", list(SCALED))
+def test_forward_matches_emulation_fp32(name):
+    w, x, g = run_case(name)
+    out = g.forward(out_dtype=torch.float32).cpu().numpy()
+    assert g.status() == (0, 0)
+    emu = oracle_ref(w, x)
+    m = metrics(out, emu)
+    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+    ex = oracle_ref(w, x, mode="exact")
+    mg, mq = metrics(out, ex), metrics(emu, ex)
+    # the GPU is exactly as accurate as the method it implements
+    assert abs(mg["relL1"] - mq["relL1"]) <= 2e-3 * max(1.0, mq["relL1"] * 10), (mg, mq)
+    assert abs(mg["cos"] - mq["cos"]) <= 1e-4, (mg, mq)
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill", "varlen"])
+def test_forward_low_precision_output(name):
+    w, x, g = run_case(name)
+    out = g.forward()
+    assert out.dtype == x["q"].dtype
+    got = out.float().cpu().numpy().astype(np.float64)
+    emu = oracle_ref(w, x)
+    want_bits = oracle.round_output(emu, W.dtype_code(w))
+    want = torch.from_numpy(want_bits.view(np.int16)).view(x["q"].dtype).double().numpy()
+    mant = 7 if w.dtype == "bf16" else 10
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 1e-30))) - mant)
+    assert np.all(np.abs(got - want) <= ulp * 1.0001 + 1e-30)
+    assert metrics(got, want)["relL1"] <= REL_L1
+
+
+def test_dense_entry_point_equals_varlen():
+    w, x, g = run_case("prefill")
+    # prefill_s has two sequences of different length: use a uniform one for the dense call
+    w2 = W.scaled(W.PREFILL, (384, 384), (384, 384), hq=4, hkv=2, name="dense_eq")
+    x2 = W.make_inputs(w2)
+    g2 = GpuRun(w2, x2)
+    a = g2.forward(out_dtype=torch.float32)
+    q = x2["q"].view(2, 384, 4, 128).cuda()
+    k = x2["k"].view(2, 384, 2, 128).cuda()
+    v = x2["v"].view(2, 384, 2, 128).cuda()
+    b = S.attn_fwd(q, k, v, causal=True, out_dtype=torch.float32)
+    assert torch.equal(a.view(2, 384, 4, 128), b)
+
+
+def test_repeatable_bit_identical():
+    w, x, g = run_case("varlen")
+    a = g.forward(out_dtype=torch.float32)
+    b = g.forward(out_dtype=torch.float32)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ edge cases
+EDGE = [
+    # (nq, nkv, hq, hkv, d, causal, dtype)
+    ((1,), (1,), 1, 1, 64, False, "fp16"),
+    ((1,), (1000,), 2, 1, 128, True, "bf16"),      # one query sees every key (bottom-right)
+    ((300,), (100,), 2, 2, 128, True, "bf16"),     # rows with no visible key output 0
+    ((100,), (300,), 2, 2, 64, True, "fp16"),
+    ((129, 0, 5), (0, 64, 257), 4, 2, 128, False, "bf16"),  # empty sequences
+    ((200,), (200,), 8, 1, 32, True, "bf16"),      # D0 = 32, GQA 8
+    ((200,), (333,), 2, 2, 80, False, "fp16"),     # D0 = 80
+    ((150,), (150,), 2, 2, 96, True, "bf16"),
+    ((130,), (260,), 2, 2, 112, False, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[f"e{i}" for i in range(len(EDGE))])
+def test_edge_cases(case):
+    nq, nkv, hq, hkv, d, causal, dt = case
+    w = W.Workload("edge", nq, nkv, hq, hkv, d, dt, causal, "kbias9", 31, varlen=True)
+    x = W.make_inputs(w)
+    g = GpuRun(w, x)
+    out = g.forward(out_dtype=torch.float32).cpu().numpy()
+    assert g.status() == (0, 0)
+    emu = oracle_ref(w, x)
+    m = metrics(out, emu)
+    if np.abs(emu).sum() == 0:
+        assert np.all(out == 0)
+    else:
+        assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+    # rows with no visible key are exactly zero
+    for b in range(w.batch):
+        for i in range(w.nq[b]):
+            if w.nkv[b] == 0 or (causal and i + w.nkv[b] - w.nq[b] < 0):
+                assert np.all(out[x["cu_q"][b] + i] == 0)
+
+
+def test_sm_scale_argument():
+    w = W.scaled(W.TINY, (200,), (300,), hq=2, hkv=2)
+    x = W.make_inputs(w)
+    g = GpuRun(w, x, sm_scale=0.05)
+    out = g.forward(out_dtype=torch.float32).cpu().numpy()
+    emu = oracle.attention_emulated(bits(x["q"]), bits(x["k"]), bits(x["v"]), 0, x["cu_q"],
+                                    x["cu_kv"], 2, 2, 64, False, 0.05)
+    m = metrics(out, emu)
+    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+
+
+# ------------------------------------------------------------------ full-size workloads
+@pytest.mark.parametrize("wl", [W.PREFILL, W.GQA_LONG, W.VIDEO_DIT, W.VARLEN],
+                         ids=["prefill", "gqa_long", "video_dit", "varlen"])
+def test_full_size_sampled_units(wl):
+    """Full-size workloads, launched as the benchmark launches them; the oracle computes
+    >= 32 seeded (sequence, head, Q block) units including every last partial block, the
+    first block and a causal-diagonal block."""
+    x = W.make_inputs(wl)
+    g = GpuRun(wl, x)
+    out = g.forward(out_dtype=torch.float32)
+    assert g.status() == (0, 0)
+    units = units_sample(wl, 32, seed=wl.seed)
+    emu = oracle_ref(wl, x, units=units)
+    toks, heads = unit_rows(wl, x["cu_q"], units)
+    got = out[torch.from_numpy(toks).cuda(), torch.from_numpy(heads).cuda()].cpu().numpy()
+    m = metrics(got, emu[toks, heads])
+    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+
+
+# ------------------------------------------------------------------ failure detection
+def test_bounded_wait_reports_timeout_and_context_survives():
+    w = W.TINY
+    x = W.make_inputs(w)
+    g = GpuRun(w, x)
+    g.prepass()
+    S.debug_timeout(g.ws, 1, 2, 2, 256, 256, 64)
+    code, raw = g.status()
+    assert code == -5 and (raw & 0xFF00) == 0x100, (code, hex(raw))
+    # the context is still usable: a normal forward afterwards is clean and correct
+    out = g.forward(out_dtype=torch.float32).cpu().numpy()
+    assert g.status() == (0, 0)
+    m = metrics(out, oracle_ref(w, x))
+    assert m["relL1"] <= REL_L1, m
