@@ -1,0 +1,364 @@
+"""Benchmark of the SageAttention2 quantized attention forward on GB300.
+
+One step = the whole hot path on one batch: the smoothing/quantization prepass and the
+fused attention kernel, through the C ABI, inputs resident in HBM. Default workload: the
+GQA long-context causal case (B=1, Hq=32, Hkv=8, N=32768, D=128, bf16), the one the metric
+is quoted on (N in 8k-32k, D=128). Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (the plain C emulation of the same pipeline) on a
+bounded sample of the same workload, on this machine's host cores.
+
+Multi-GPU (torchrun): the path shards by independent (sequence, kv head) problems with no
+exchange, so each rank runs its own replica of the workload ("weak" scaling); ranks meet
+at a barrier around the timed region and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_exact_attention_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention TOPS (4BHNqNkvD/t) at N=8k-32k, D=128; % of GB300 dense INT8/FP8 peak"
+WORKLOADS = {w.name: w for w in W.ALL}
+WORKLOADS.update({"gqa_long": W.GQA_LONG, "prefill": W.PREFILL, "video_dit": W.VIDEO_DIT,
+                  "varlen": W.VARLEN, "tiny": W.TINY})
+FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor ratio (GB300)
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="gqa_long", choices=sorted(WORKLOADS))
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(ops_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput in TOPS: the work of every rank over the slowest rank's time."""
+    return ops_per_rank * world / seconds_max / 1e12
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample(w: W.Workload, x: dict, n_units: int, seed: int = 0):
+    """A bounded sample of the workload for the CPU oracle: n_units (sequence, head, Q block)
+    units spread over the Q blocks, with the exact number of operations they contain."""
+    rng = np.random.default_rng(seed)
+    total_units = sum((n + 127) // 128 for n in w.nq) * w.hq
+    chosen = set()
+    while len(chosen) < min(n_units, total_units):
+        b = int(rng.integers(w.batch))
+        nqb = (w.nq[b] + 127) // 128
+        if nqb:
+            chosen.add((b, int(rng.integers(w.hq)), int(rng.integers(nqb))))
+    units, ops = sorted(chosen), 0.0
+    for b, h, qb in units:
+        r0, r1 = qb * 128, min(w.nq[b], qb * 128 + 128)
+        for i in range(r0, r1):
+            vis = w.nkv[b] if not w.causal else max(0, min(w.nkv[b], i + w.nkv[b] - w.nq[b] + 1))
+            ops += 4.0 * vis * w.d
+    return units, ops
+
+
+def run_oracle_sample(w: W.Workload, x: dict, units):
+    import oracle
+    oracle.build()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.attention_emulated(bits(x["q"]), bits(x["k"]), bits(x["v"]), W.dtype_code(w),
+                              x["cu_q"], x["cu_kv"], w.hq, w.hkv, w.d, w.causal, units=units)
+    return time.perf_counter() - t0, oracle.num_threads()
+
+
+def sample_size(w: W.Workload) -> int:
+    return 12 if max(w.nkv) >= 16384 else 32
+
+
+# ------------------------------------------------------------------ our implementation
+def run_ours(args, rank, world, local):
+    import bit_exact_attention_gb300 as S
+    from bit_exact_attention_gb300 import _lib
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    x = W.make_inputs(w)
+    B, hq, hkv, d = w.batch, w.hq, w.hkv, w.d
+    max_nq, max_nkv, tq, tkv = max(w.nq), max(w.nkv), sum(w.nq), sum(w.nkv)
+    q, k, v = (x[n].to(dev) for n in "qkv")
+    cu_q = torch.tensor(x["cu_q"], dtype=torch.int32, device=dev)
+    cu_kv = torch.tensor(x["cu_kv"], dtype=torch.int32, device=dev)
+    out = torch.empty(tq, hq, d, dtype=q.dtype, device=dev)
+    nws = S.workspace_size(B, hq, hkv, max_nq, max_nkv, d, tq, tkv)
+    ws = S.alloc_workspace(nws, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ops = w.metric_ops()
+
+    def prepass():
+        S.prepass_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, ws, causal=w.causal, stream=stream)
+
+    def attention():
+        S.attention_varlen(out, ws, cu_q, cu_kv, hkv, max_nq, max_nkv, tkv, causal=w.causal,
+                           stream=stream)
+
+    for _ in range(args.warmup):
+        prepass()
+        attention()
+    torch.cuda.synchronize(dev)
+    rc, raw = S.device_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {rc} {raw:#x}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # evict L2 between steps (outside the timed events)
+        ev[i][0].record(stream)
+        prepass()
+        ev[i][1].record(stream)
+        attention()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    rc, raw = S.device_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"device status after the timed steps: {rc} {raw:#x}")
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    att_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [a + b for a, b in zip(pre_ms, att_ms)]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    value = aggregate_value(ops * args.steps, total_s, world)
+    ms_per_step = total_s * 1e3 / args.steps
+    att_mean = statistics.mean(att_ms)
+    pre_mean = statistics.mean(pre_ms)
+    kernels_per_step = 7  # prepass: 6 kernels; attention: 1
+
+    # end to end through the public API: pinned host inputs in, host output back
+    e2e = None
+    if not args.no_e2e:
+        hq_, hk_, hv_ = (x[n].pin_memory() for n in "qkv")
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        for _ in range(2):
+            q.copy_(hq_, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv_, non_blocking=True)
+            S.attn_fwd_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, causal=w.causal, out=out,
+                              workspace=ws, stream=stream)
+            hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            es[i][0].record(stream)
+            q.copy_(hq_, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv_, non_blocking=True)
+            S.attn_fwd_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, causal=w.causal, out=out,
+                              workspace=ws, stream=stream)
+            hout.copy_(out, non_blocking=True)
+            es[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in es) / 1e3, world, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
+        d2h = hout.numel() * hout.element_size()
+        e2e = {"value": aggregate_value(ops * args.steps, e2e_s, world), "unit": "TOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_s * 1e3 / args.steps}
+
+    bf16_burst, bf16_sust, peak_src = measured_peaks()
+    peak = bf16_burst * FP8_OVER_BF16
+    achieved = ops / (att_mean / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "attn_fwd", "peak_source": f"{peak_src} bf16 burst x {FP8_OVER_BF16} (e4m3)",
+                "frac_of_sustained": round(achieved / (bf16_sust * FP8_OVER_BF16), 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        units, sops = oracle_sample(w, x, sample_size(w))
+        secs, cores = run_oracle_sample(w, x, units)
+        cpu = {"value": sops / secs / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
+               "sample": f"{len(units)} seeded (sequence, head, 128-row Q block) units of "
+                         f"{w.name} ({sops:.3e} ops); the oracle's quantization of the full "
+                         f"inputs is inside the {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded, distributions of the workload description)",
+            "config": {"workload": w.name, "batch": B, "hq": hq, "hkv": hkv, "nq": list(w.nq),
+                       "nkv": list(w.nkv), "d": d, "causal": w.causal, "in_dtype": w.dtype,
+                       "metric_ops_per_step": ops, "parallelism": f"replicas x{world}",
+                       "l2": "flushed between timed steps (256 MB write)"},
+            "kernel_only_tops": round(ops / (att_mean / 1e3) / 1e12, 3),
+            "prepass_ms": round(pre_mean, 4), "attention_ms": round(att_mean, 4),
+            "wall_s": round(t_wall, 4),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ the oracle arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    x = W.make_inputs(w)
+    units, sops = oracle_sample(w, x, max(2, sample_size(w) // 4))
+    for _ in range(args.warmup):  # untimed, on a single unit to keep the run short
+        run_oracle_sample(w, x, units[:1])
+    times, cores = [], 1
+    for i in range(args.steps):
+        s, cores = run_oracle_sample(w, x, units)
+        times.append(s)
+    total = sum(times)
+    value = sops * args.steps / total / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": w.name, "sample_units": len(units)},
+            "cpu_baseline": {"value": value, "unit": "TOPS", "kind": "oracle", "cores": cores,
+                             "sample": f"{len(units)} (sequence, head, Q block) units per step, "
+                                       f"{sops:.3e} ops"},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    init_dist(world, "nccl" if torch.cuda.is_available() else "gloo")
+    run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
