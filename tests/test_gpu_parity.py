@@ -185,9 +185,13 @@ def test_forward_low_precision_output(name):
     emu = oracle_ref(w, x)
     want_bits = oracle.round_output(emu, W.dtype_code(w))
     want = torch.from_numpy(want_bits.view(np.int16)).view(x["q"].dtype).double().numpy()
+    # The FP32 result may sit up to MAX_ABS from the emulation; rounding both to the
+    # output dtype adds at most one unit in the last place of the larger of the two.
     mant = 7 if w.dtype == "bf16" else 10
-    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 1e-30))) - mant)
-    assert np.all(np.abs(got - want) <= ulp * 1.0001 + 1e-30)
+    mag = np.maximum(np.abs(want), np.abs(got))
+    ulp = np.exp2(np.floor(np.log2(np.maximum(mag, 1e-30))) - mant)
+    excess = np.abs(got - want) - (MAX_ABS + ulp)
+    assert excess.max() <= 0, f"{int((excess > 0).sum())} elements beyond MAX_ABS + 1 ulp"
     assert metrics(got, want)["relL1"] <= REL_L1
 
 
