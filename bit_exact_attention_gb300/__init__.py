@@ -21,9 +21,11 @@ from ._lib import BF16, FP16, FP32, Sage2Error, WsLayout  # noqa: F401
 
 __all__ = ["attn_fwd", "attn_fwd_varlen", "prepass", "attention", "prepass_varlen",
            "attention_varlen", "workspace_size", "workspace_layout", "device_status",
-           "alloc_workspace", "debug_tile", "debug_timeout", "Sage2Error", "load_library"]
+           "alloc_workspace", "debug_tile", "debug_timeout", "Sage2Error", "load_library",
+           "attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES"]
 
 _DT = {torch.float16: FP16, torch.bfloat16: BF16, torch.float32: FP32}
+NOALLOC_SCRATCH_BYTES = 64 << 20  # SAGE2_NOALLOC_SCRATCH_BYTES in include/sage2_attn.h
 
 
 def load_library():
@@ -199,3 +201,19 @@ def debug_timeout(workspace, B, Hq, Hkv, Nq, Nkv, D, stream=None):
     _lib.check(_lib.lib().sage2_debug_timeout(B, Hq, Hkv, Nq, Nkv, D, _ptr(workspace),
                                               workspace.numel(), _stream(stream)),
                "sage2_debug_timeout")
+
+
+def attn_fwd_noalloc(q, k, v, out, causal=False, sm_scale=0.0, stream=None):
+    """Forward that allocates no device memory, for callers that cannot allocate (engines
+    whose runtime owns every device allocation, allocation-free latency-critical loops).
+    Uses the library's built-in scratch (NOALLOC_SCRATCH_BYTES per GPU, held until exit)
+    instead of a workspace; ``out`` must be provided. Calls share that scratch, so calls that
+    overlap on the GPU race; keep them ordered."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _dev(t, n)
+    B, Nq, Hq, D = q.shape
+    _, Nkv, Hkv, _ = k.shape
+    _lib.check(_lib.lib().sage2_attn_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _code(q.dtype), _code(out.dtype), B, Hq, Hkv, Nq,
+        Nkv, D, int(bool(causal)), float(sm_scale), _stream(stream)), "sage2_attn_fwd_noalloc")
+    return out

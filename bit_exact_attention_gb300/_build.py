@@ -1,6 +1,6 @@
 """Builds the CUDA library (libsage2_attn.so) in-tree with nvcc for sm_103a.
 
-Three translation units compile in parallel; the CUDA runtime is linked statically, and the
+The translation units compile in parallel; the CUDA runtime is linked statically, and the
 driver's tensor-map encoder is looked up at run time, so the library needs no libcuda at link
 time and loads on a machine without a GPU.
 """
@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsage2_attn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["sage2_api.cu", "sage2_prepass.cu", "sage2_attention.cu"]
+SOURCES = ["sage2_api.cu", "sage2_prepass.cu", "sage2_attention.cu", "sage2_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -57,6 +57,7 @@ def _declare(lib):
         "sage2_device_status": ([P, P, ctypes.POINTER(i)], i),
         "sage2_debug_tile": ([P, P, i, i, i, i, i, i, i, i, i, f, P, sz, i, i, i, i, P, P, P, P], i),
         "sage2_debug_timeout": ([i, i, i, i, i, i, P, sz, P], i),
+        "sage2_attn_fwd_noalloc": ([P, P, P, P, i, i, i, i, i, i, i, i, i, f, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

@@ -152,6 +152,26 @@ int sage2_debug_tile(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, i
 int sage2_debug_timeout(int B, int Hq, int Hkv, int Nq, int Nkv, int D, const void *workspace,
                         size_t workspace_bytes, void *stream);
 
+/* Forward without any device allocation. No counterpart in the paper: this exists for
+ * callers that cannot give the library a workspace -- runtimes that hand out device memory
+ * only from their own pre-planned pools and forbid allocation calls from third-party code,
+ * and latency-critical loops where an allocation call (which may synchronize the device) is
+ * not allowed. Same arguments and results as sage2_attn_fwd, minus the workspace: the
+ * library uses a fixed scratch array of SAGE2_NOALLOC_SCRATCH_BYTES that every GPU loading
+ * the library holds until the process exits.
+ *   - Returns SAGE2_EWORKSPACE, before queuing any work, when sage2_workspace_size() of the
+ *     problem exceeds SAGE2_NOALLOC_SCRATCH_BYTES; other argument errors as sage2_attn_fwd.
+ *   - The first call on a device looks up the scratch address with that device current;
+ *     make that first call before any stream capture.
+ *   - All calls share the scratch, which keeps the last call's contents (each call rewrites
+ *     what it reads and clears its status word). Calls that overlap on the GPU race and
+ *     corrupt each other; order them (one stream, or explicit synchronization).
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no allocating library routine. */
+#define SAGE2_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int sage2_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *out, int in_dtype,
+                           int out_dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                           int causal, float sm_scale, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
