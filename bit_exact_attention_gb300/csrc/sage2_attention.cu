@@ -1,18 +1,20 @@
 // sage2_attention.cu -- the fused SageAttention2 attention kernel for sm_103a.
 //
-// One CTA per (sequence, q head, 128-row Q tile); six warps:
-//   warp 4 (one lane)   TMA producer: the Q-code tile once, then per 128-key KV tile the
-//                       K-code tile, the transposed V-code tile, 128 DeltaS*c values and the
-//                       4 K scales, into a ST-stage shared-memory ring.
-//   warp 5 (one lane)   MMA issuer (tcgen05, kind::f8f6f4, e4m3 x e4m3 -> f32):
-//                       S = Qcode Kcode^T into tensor memory (two S buffers, so the next
-//                       tile's S is computed while the softmax works on this one), then
-//                       R = P~ Vcode with P~ read from tensor memory.
-//   warps 0-3           softmax and fold, one accumulator row per thread (the TMEM lane of
-//                       that row): dequantize + DeltaS in one FMA per element, online softmax
-//                       in base 2, P~ = e4m3(448 P) written back to tensor memory, then the
-//                       fresh FP32 partial R folded into the FP32 output accumulator held in
-//                       registers (O = alpha O + R), and the epilogue.
+// One CTA per (sequence, q head, 128-row Q tile); ten warps:
+//   warps 0-3  softmax: thread t of warp w owns accumulator row 32w+t (its TMEM lane). Per
+//              128-key tile it loads the whole S row from tensor memory in one instruction,
+//              dequantizes and adds DeltaS with one FMA per element, takes the row maximum,
+//              computes P448 = 2^(S' - m + log2 448) in base 2, writes P~ = e4m3(P448) back to
+//              tensor memory (the A operand of the P~V MMA) and hands alpha = 2^(m_old - m_new)
+//              to the fold warps.
+//   warps 4-7  fold + epilogue: thread t of warp 4+w owns row 32w+t of the FP32 output in
+//              registers and folds the fresh per-tile partial: O = alpha O + R. At the end it
+//              divides by the row sum and writes the output row.
+//   warp 8     TMA producer (one lane): Q codes once, then per KV tile the K codes, transposed
+//              V codes, 128 DeltaS*c values and 4 K scales into an ST-stage ring.
+//   warp 9     MMA issuer (one lane) and tensor-memory owner: S = Qcode Kcode^T
+//              (tcgen05 kind::f8f6f4, e4m3 x e4m3 -> f32, both operands from shared memory),
+//              R = P~ Vcode (A from tensor memory), into double-buffered S and R.
 // Method (SageAttention2 pages): INT4-grid Q and K codes with per-thread-group scales; P~ and
 // V in e4m3; two-level accumulation of P~V ("SageAttention2: Efficient Attention with Thorough
 // Outlier Smoothing and Per-thread INT4 Quantization" research note, components 2 and 3;
@@ -22,8 +24,14 @@
 // at most 49 and a 128-channel dot product at most 6272 < 2^24, so the FP32 accumulator holds
 // the integer Q K^T exactly.
 //
-// Tensor memory columns (512 allocated): S0 [0,128) S1 [128,256) P~0 [256,288) P~1 [288,320)
-// R [384, 384 + Dp).
+// Tensor memory (512 columns): S0 [0,128) S1 [128,256) R0 [256, 256+Dp) R1 [384, 384+Dp);
+// P~ of tile j overwrites the first 32 columns of its S buffer once the softmax has read S.
+//
+// Pipeline per KV tile j (sb = j % 2): the MMA warp issues QK(j+1) as soon as PV(j-1) has
+// finished reading P~(j-1) from S[(j+1)%2], so the tensor core computes the next S while the
+// softmax works on this one; PV(j) waits for P~(j) and for the fold of R(j-2). The alpha of
+// tile j travels through a 4-deep shared ring: the softmax cannot run more than three tiles
+// ahead of the fold (tile j+4 needs PV(j+2), which needs the fold of tile j).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -35,14 +43,14 @@
 namespace sage2 {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColP0 = 256, kColP1 = 288, kColR = 384;
+constexpr int kThreads = 320;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColR0 = 256, kColR1 = 384;
 constexpr uint32_t kTmemCols = 512;
 
 // wait-site ids reported in the status word
 enum : int {
   kSiteQ = 1, kSiteKvFull = 2, kSiteKvEmpty = 3, kSiteSFull = 4, kSitePFull = 5, kSiteRFull = 6,
-  kSiteRFree = 7, kSiteKvFullSm = 8, kSiteDrain = 9
+  kSiteRFree = 7, kSiteKvFullSm = 8, kSiteAFull = 9, kSiteLFull = 10
 };
 
 struct AttnArgs {
@@ -62,8 +70,11 @@ struct SmemPlan {
   static constexpr int kV = kK + ST * 128 * DP;
   static constexpr int kDsc = kV + ST * DP * 128;
   static constexpr int kSk = kDsc + ST * 512;
-  static constexpr int kBar = kSk + ST * 16;
-  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 3;  // q, full/empty, s, p, r_full r_free drain
+  static constexpr int kAlpha = kSk + ST * 16;         // float [4][128]
+  static constexpr int kLsum = kAlpha + 4 * 128 * 4;  // float [128]
+  static constexpr int kBar = kLsum + 128 * 4;
+  // q, full[ST], empty[ST], s[2], p[2], r_full[2], r_free[2], a[4], l, drain
+  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 2 + 2 + 4 + 1 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
@@ -75,38 +86,6 @@ __device__ bool drain_wait(uint64_t *bar, uint32_t parity) {
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > SAGE2_WAIT_NS) return false;
   return true;
-}
-
-template <bool MASK>
-__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], float mult, const float *dsc,
-                                           int col0, int lim, float mx) {
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    float s = __fmaf_rn(__uint_as_float(v[e]), mult, dsc[col0 + e]);
-    if (MASK) s = (col0 + e <= lim) ? s : -INFINITY;
-    mx = fmaxf(mx, s);
-  }
-  return mx;
-}
-
-template <bool MASK>
-__device__ __forceinline__ float chunk_probs(const uint32_t (&v)[32], float mult, const float *dsc,
-                                             int col0, int lim, float m448, uint32_t (&pk)[8]) {
-  float ps = 0.f;
-#pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    float p[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float s = __fmaf_rn(__uint_as_float(v[e + u]), mult, dsc[col0 + e + u]);
-      float pv = ex2_approx(__fsub_rn(s, m448));
-      if (MASK) pv = (col0 + e + u <= lim) ? pv : 0.f;
-      p[u] = pv;
-      ps += pv;
-    }
-    pk[e / 4] = cvt_e4m3x2(p[0], p[1]) | (cvt_e4m3x2(p[2], p[3]) << 16);
-  }
-  return ps;
 }
 
 template <int DP, int ST, bool DBG>
@@ -150,19 +129,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   uint8_t *sQ = smem + P::kQ;
+  float *alpha_ring = reinterpret_cast<float *>(smem + P::kAlpha);
+  float *lsum = reinterpret_cast<float *>(smem + P::kLsum);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::kBar);
   uint64_t *q_full = bars;
   uint64_t *kv_full = bars + 1;
-  uint64_t *kv_empty = bars + 1 + ST;
-  uint64_t *s_full = bars + 1 + 2 * ST;
+  uint64_t *kv_empty = kv_full + ST;
+  uint64_t *s_full = kv_empty + ST;
   uint64_t *p_full = s_full + 2;
   uint64_t *r_full = p_full + 2;
-  uint64_t *r_free = r_full + 1;
-  uint64_t *drain = r_free + 1;
+  uint64_t *r_free = r_full + 2;
+  uint64_t *a_full = r_free + 2;
+  uint64_t *l_full = a_full + 4;
+  uint64_t *drain = l_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kMisc + 4);
 
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < ST; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -171,9 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
+      mbar_init(&r_full[i], 1);
+      mbar_init(&r_free[i], 4);
     }
-    mbar_init(r_full, 1);
-    mbar_init(r_free, 4);
+    for (int i = 0; i < 4; ++i) mbar_init(&a_full[i], 4);
+    mbar_init(l_full, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -181,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -191,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
   const AbortCtx ab{abort_flag, a.status};
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const int yq = hq * a.L.Tq + s.qpad0 + qt * kBQ;
@@ -229,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_wait(&kv_full[n % ST], (n / ST) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
@@ -253,31 +238,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < T; ++j) {
         if (j + 1 < T) {
           ok = mbar_wait(&kv_full[(j + 1) % ST], ((j + 1) / ST) & 1, ab, kSiteKvFull);
+          // S[(j+1)%2] still holds P~(j-1): PV(j-1) must have finished reading it
+          if (ok && j >= 1) ok = mbar_wait(&r_full[(j - 1) & 1], ((j - 1) >> 1) & 1, ab, kSiteRFull);
           if (!ok) break;
           tc_fence_after();
           issue_qk(j + 1);
         }
         ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, ab, kSitePFull);
+        if (ok && j >= 2) ok = mbar_wait(&r_free[j & 1], ((j - 2) >> 1) & 1, ab, kSiteRFree);
         if (!ok) break;
-        if (j >= 1) {
-          ok = mbar_wait(r_free, (j - 1) & 1, ab, kSiteRFree);
-          if (!ok) break;
-        }
         tc_fence_after();
         const int st = j % ST;
         const uint64_t vdesc = sdesc_kmajor(smem_u32(smem + P::kV + st * DP * 128), 128);
-        const uint32_t aP = tbase + ((j & 1) ? kColP1 : kColP0);
+        const uint32_t aP = tbase + ((j & 1) ? kColS1 : kColS0);
+        const uint32_t dR = tbase + ((j & 1) ? kColR1 : kColR0);
 #pragma unroll
         for (int kk = 0; kk < kBKV / 32; ++kk)
-          mma_e4m3_ts(tbase + kColR, aP + kk * 8, vdesc + (uint64_t)(kk * 2), idesc_pv, kk > 0);
-        mma_commit(r_full);
+          mma_e4m3_ts(dR, aP + kk * 8, vdesc + (uint64_t)(kk * 2), idesc_pv, kk > 0);
+        mma_commit(&r_full[j & 1]);
         mma_commit(&kv_empty[st]);
       }
       mma_commit(drain);  // every MMA issued above completes before tensor memory is freed
       drain_wait(drain, 0);
     }
-  } else {
-    // ------------------------------------------------------------ softmax + fold (warps 0-3)
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax (warps 0-3)
     const int row = warp * 32 + lane;
     const int i = qt * kBQ + row;
     const bool row_ok = i < s.nq;
@@ -287,52 +272,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int last_key = g.causal ? min(i + (s.nkv - s.nq), s.nkv - 1) : s.nkv - 1;
     const float L32 = 8.8073549220576041f;  // fl32(log2(448))
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float O[DP];
-#pragma unroll
-    for (int d = 0; d < DP; ++d) O[d] = 0.f;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int sb = j & 1, st = j % ST;
-      ok = mbar_wait(&s_full[sb], (j >> 1) & 1, ab, kSiteSFull);
-      if (!ok) break;
-      ok = mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm);
-      if (!ok) break;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, ab, kSiteSFull)) break;
+      if (!mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm)) break;
       tc_fence_after();
       const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 512);
       const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
-      const int lim = last_key - j * kBKV;
-      const bool full = lim >= kBKV - 1;
+      const int lim = last_key - j * kBKV;  // columns 0..lim are visible to this row
       const uint32_t tS = tbase + lane_base + (sb ? kColS1 : kColS0);
-      const uint32_t tP = tbase + lane_base + (sb ? kColP1 : kColP0);
-      float mult[4];
+      uint32_t v[128];
+      tmem_ld128(tS, v);
+      if (DBG && j == a.dbg.kt) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) mult[c] = __fmul_rn(sqc, skv[c]);
-      // pass A: the row maximum of the dequantized, corrected logits (log2 units)
-      float mx = -INFINITY;
+        for (int e = 0; e < 128; ++e) a.dbg.s_out[row * 128 + e] = __uint_as_float(v[e]);
+      }
+      float x[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32_wait(tS + c * 32, v);
-        if (DBG && j == a.dbg.kt) {
+        const float mult = __fmul_rn(sqc, skv[c]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a.dbg.s_out[row * 128 + c * 32 + e] = __uint_as_float(v[e]);
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4 *>(dsc + c * 32 + e);
+          const int k0 = c * 32 + e;
+          fma2(x[k0], x[k0 + 1], __uint_as_float(v[k0]), __uint_as_float(v[k0 + 1]), mult, mult,
+               d4.x, d4.y);
+          fma2(x[k0 + 2], x[k0 + 3], __uint_as_float(v[k0 + 2]), __uint_as_float(v[k0 + 3]), mult,
+               mult, d4.z, d4.w);
         }
-        mx = full ? chunk_max<false>(v, mult[c], dsc, c * 32, lim, mx)
-                  : chunk_max<true>(v, mult[c], dsc, c * 32, lim, mx);
       }
-      const float m_new = fmaxf(m, mx);
+      if (lim < kBKV - 1) {  // diagonal / ragged tile: hide the keys this row does not see
+#pragma unroll
+        for (int e = 0; e < 128; ++e) x[e] = (e <= lim) ? x[e] : -INFINITY;
+      }
+      float mx = m;
+#pragma unroll
+      for (int e = 0; e < 128; e += 2) mx = max3(mx, x[e], x[e + 1]);
+      const float m_new = mx;
       const float m448 = (m_new == -INFINITY) ? 0.f : __fsub_rn(m_new, L32);
       const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(__fsub_rn(m, m_new));
-      // pass B: P448 = 2^(S' - m + log2 448), P~ = e4m3(P448) into tensor memory
-      float ps = 0.f;
+      // P448 = 2^(S' - m448); masked keys have S' = -inf and give 0
+      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32], pk[8];
-        tmem_ld32_wait(tS + c * 32, v);
-        ps += full ? chunk_probs<false>(v, mult[c], dsc, c * 32, lim, m448, pk)
-                   : chunk_probs<true>(v, mult[c], dsc, c * 32, lim, m448, pk);
-        tmem_st8(tP + c * 8, pk);
+      for (int c = 0; c < 4; ++c) {  // 32 keys -> 8 words of P~ per chunk
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = c * 32; e < c * 32 + 32; e += 4) {
+          float t0, t1, t2, t3;
+          add2(t0, t1, x[e], x[e + 1], -m448, -m448);
+          add2(t2, t3, x[e + 2], x[e + 3], -m448, -m448);
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1), p2 = ex2_approx(t2),
+                      p3 = ex2_approx(t3);
+          add2(ps0, ps1, ps0, ps1, p0, p1);
+          add2(ps0, ps1, ps0, ps1, p2, p3);
+          pk[(e - c * 32) / 4] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
+        }
+        tmem_st8(tS + c * 8, pk);
         if (DBG && j == a.dbg.kt) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -341,31 +337,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
+      alpha_ring[(j & 3) * 128 + row] = alpha;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
-      l = __fmaf_rn(alpha, l, ps);
+      if (lane == 0) {
+        mbar_arrive(&p_full[sb]);
+        mbar_arrive(&a_full[j & 3]);
+      }
+      l = __fmaf_rn(alpha, l, __fadd_rn(ps0, ps1));
       m = m_new;
-      // fold the fresh FP32 partial of this KV tile: O = alpha O + R
-      ok = mbar_wait(r_full, j & 1, ab, kSiteRFull);
+    }
+    lsum[row] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(l_full);
+  } else {
+    // ------------------------------------------------------------ fold + epilogue (warps 4-7)
+    const int q4 = warp - 4;
+    const int row = q4 * 32 + lane;
+    const int i = qt * kBQ + row;
+    const bool row_ok = i < s.nq;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    float O[DP];
+#pragma unroll
+    for (int d = 0; d < DP; ++d) O[d] = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(&a_full[j & 3], (j >> 2) & 1, ab, kSiteAFull);
+      if (!ok) break;
+      const float alpha = alpha_ring[(j & 3) * 128 + row];
+      ok = mbar_wait(&r_full[sb], (j >> 1) & 1, ab, kSiteRFull);
       if (!ok) break;
       tc_fence_after();
+      const uint32_t tR = tbase + lane_base + (sb ? kColR1 : kColR0);
 #pragma unroll
-      for (int c = 0; c < DP / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32_wait(tbase + lane_base + kColR + c * 32, v);
+      for (int c = 0; c < DP / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16_wait(tR + c * 16, v);
         if (DBG && j == a.dbg.kt) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a.dbg.r_out[row * DP + c * 32 + e] = __uint_as_float(v[e]);
+          for (int e = 0; e < 16; ++e) a.dbg.r_out[row * DP + c * 16 + e] = __uint_as_float(v[e]);
         }
 #pragma unroll
-        for (int e = 0; e < 32; ++e) O[c * 32 + e] = __fmaf_rn(alpha, O[c * 32 + e], __uint_as_float(v[e]));
+        for (int e = 0; e < 16; e += 2)
+          fma2(O[c * 16 + e], O[c * 16 + e + 1], alpha, alpha, O[c * 16 + e], O[c * 16 + e + 1],
+               __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(r_free);
+      if (lane == 0) mbar_arrive(&r_free[sb]);
     }
+    if (ok) ok = mbar_wait(l_full, 0, ab, kSiteLFull);
     // ------------------------------------------------------------ epilogue
     if (ok && row_ok && !*abort_flag) {
+      const float l = lsum[row];
       const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
       const float *svp = a.vscale + ((size_t)b * g.Hkv + hk) * DP;
       const size_t o = (out_row0 + (size_t)row * g.Hq) * g.D0;
@@ -406,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tbase, kTmemCols);
+  if (warp == 9) tmem_dealloc(tbase, kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side

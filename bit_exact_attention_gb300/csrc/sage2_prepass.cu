@@ -14,7 +14,7 @@
 //   4. q_quant: per block of 128 rows the mean qmean; Q~ = fl32(Q - qmean); one scale per
 //      row; codes as for K.
 //   5. delta_s: DeltaS = qmean . K~ in FP32, one fused multiply-add per channel in channel
-//      order, stored pre-multiplied by c = log2(e) * sm_scale.
+//      order (register-blocked tiles), stored pre-multiplied by c = log2(e) * sm_scale.
 // Every padded position (channels D0..Dp, tokens past a sequence end up to its 128-row
 // boundary) is written with zero codes and zero scales.
 #include <cuda_bf16.h>
@@ -348,71 +348,125 @@ __global__ void __launch_bounds__(128) q_quant(PrepassArgs a) {
 }
 
 // ------------------------------------------------------------------ 5. DeltaS
-// grid (ceil(max_nkv / 128), Hkv, B), block 128: thread j holds the smoothed key
-// kt * 128 + j and produces its DeltaS for every (q head of the group, Q block) that visits
-// this KV tile; four Q blocks at a time for independent FMA chains.
+// A small FP32 GEMM per (sequence, kv head): rows are the (Q block, q head of the group)
+// pairs, ordered Q-block-major (r = qb * g + head), columns the keys, inner dimension the
+// channels. grid (key tiles of 128, row tiles of 128, B * Hkv), block 256. Thread (tr, tk)
+// owns rows 8tr..8tr+7 and keys 8tk..8tk+7; channels are staged 32 at a time in shared memory,
+// transposed, and every output is one FMA chain in increasing channel order (the same
+// operation sequence as the definition, so the result is bit-identical to it). Causal: a
+// (row tile, key tile) pair that no row of the tile visits is skipped; rows that do not visit
+// the key tile are not written.
+constexpr int kDsRows = 128, kDsKeys = 128, kDsChan = 32;
+
 template <int DP>
-__global__ void __launch_bounds__(128) delta_s(PrepassArgs a) {
+__global__ void __launch_bounds__(256) delta_s(PrepassArgs a) {
+  __shared__ __align__(16) float Qs[kDsChan][kDsRows];
+  __shared__ __align__(16) float Ks[kDsChan][kDsKeys];
   const Geometry &g = a.g;
-  const int b = blockIdx.z, hk = blockIdx.y, kt = blockIdx.x;
+  const int kt = blockIdx.x, rt = blockIdx.y;
+  const int b = blockIdx.z / g.Hkv, hk = blockIdx.z % g.Hkv;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
   if (!s.ok || kt * kBKV >= s.nkv || s.nq == 0) return;
-  const int j = kt * kBKV + threadIdx.x;
-  float kt_[DP];
-  {
-    const float *mu = a.w.kmean + ((size_t)b * g.Hkv + hk) * DP;
-    const uint16_t *src = a.k + (size_t)(s.kv0 + j) * g.Hkv * g.D0 + (size_t)hk * g.D0;
+  const int grp = g.Hq / g.Hkv;
+  const int nqb = (s.nq + kBQ - 1) / kBQ;
+  const int nrows = grp * nqb;
+  const int r0 = rt * kDsRows;
+  if (r0 >= nrows) return;
+  const int qb_last = min(nrows - 1, r0 + kDsRows - 1) / grp;
+  if (g.causal && kv_tiles_for(qb_last, s.nq, s.nkv, 1) <= kt) return;
+
+  const int tid = threadIdx.x;
+  const int tr = tid >> 4, tk = tid & 15;
+  float acc[8][8];
 #pragma unroll
-    for (int d = 0; d < DP; d += 8) {
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  // loader roles: row / key = tid / 2, channel half = (tid & 1) * 16 of the 32-channel chunk
+  const int lr = tid >> 1, lh = (tid & 1) * 16;
+  const int key = kt * kBKV + lr;
+  const bool key_ok = key < s.nkv;
+  const uint16_t *ksrc = a.k + (size_t)(s.kv0 + (key_ok ? key : 0)) * g.Hkv * g.D0 + (size_t)hk * g.D0;
+  const float *mu = a.w.kmean + ((size_t)b * g.Hkv + hk) * DP;
+  const int r = r0 + lr;
+  const bool row_ok = r < nrows;
+  const float *qsrc = nullptr;
+  if (row_ok) {
+    const int qb = r / grp, hq = hk * grp + r % grp;
+    qsrc = a.w.qmean + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * DP;
+  }
+
+#pragma unroll 1
+  for (int c0 = 0; c0 < DP; c0 += kDsChan) {
+    const int cb = c0 + lh;  // first channel this thread loads
+    float kv[16], qv[16];
+    if (key_ok && cb < g.D0) {
       float x[8];
-      if (j < s.nkv && d < g.D0) {
-        unpack8(__ldg(reinterpret_cast<const uint4 *>(src + d)), a.bf16, x);
+      unpack8(__ldg(reinterpret_cast<const uint4 *>(ksrc + cb)), a.bf16, x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], mu[d + e]);
-      } else {
+      for (int e = 0; e < 8; ++e) kv[e] = __fsub_rn(x[e], mu[cb + e]);
+      unpack8(__ldg(reinterpret_cast<const uint4 *>(ksrc + cb + 8)), a.bf16, x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      for (int e = 0; e < 8; ++e) kv[8 + e] = __fsub_rn(x[e], mu[cb + 8 + e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) kv[e] = 0.f;
+    }
+    if (row_ok) {
+#pragma unroll
+      for (int e = 0; e < 16; e += 4) {
+        const float4 m4 = __ldg(reinterpret_cast<const float4 *>(qsrc + cb + e));
+        qv[e] = m4.x;
+        qv[e + 1] = m4.y;
+        qv[e + 2] = m4.z;
+        qv[e + 3] = m4.w;
       }
+    } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) kt_[d + e] = x[e];
+      for (int e = 0; e < 16; ++e) qv[e] = 0.f;
+    }
+    __syncthreads();  // the previous chunk's reads are done
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      Ks[lh + e][lr] = kv[e];
+      Qs[lh + e][lr] = qv[e];
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int d = 0; d < kDsChan; ++d) {
+      const float4 qa = *reinterpret_cast<const float4 *>(&Qs[d][tr * 8]);
+      const float4 qc = *reinterpret_cast<const float4 *>(&Qs[d][tr * 8 + 4]);
+      const float4 ka = *reinterpret_cast<const float4 *>(&Ks[d][tk * 8]);
+      const float4 kc = *reinterpret_cast<const float4 *>(&Ks[d][tk * 8 + 4]);
+      const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
+      const float kk[8] = {ka.x, ka.y, ka.z, ka.w, kc.x, kc.y, kc.z, kc.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(qq[i], kk[j], acc[i][j]);
     }
   }
-  const int nqb = (s.nq + kBQ - 1) / kBQ;
-  int qb_min = 0;
-  if (g.causal)
-    while (qb_min < nqb && kv_tiles_for(qb_min, s.nq, s.nkv, 1) <= kt) ++qb_min;
-  const int grp = g.Hq / g.Hkv;
-  const int nrows = grp * (nqb - qb_min);
-  for (int r0 = 0; r0 < nrows; r0 += 4) {
-    const float *qm[4];
-    size_t outo[4];
-    bool live[4];
+
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int r = r0 + u;
-      live[u] = r < nrows;
-      const int rr = live[u] ? r : r0;
-      const int hq = hk * grp + rr / (nqb - qb_min);
-      const int qb = qb_min + rr % (nqb - qb_min);
-      const size_t blk = (size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb;
-      qm[u] = a.w.qmean + blk * DP;
-      outo[u] = blk * a.L.nkv_pad + (size_t)kt * kBKV + threadIdx.x;
-    }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int d = 0; d < DP; d += 4) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 m4 = __ldg(reinterpret_cast<const float4 *>(qm[u] + d));
-        acc[u] = __fmaf_rn(m4.x, kt_[d], acc[u]);
-        acc[u] = __fmaf_rn(m4.y, kt_[d + 1], acc[u]);
-        acc[u] = __fmaf_rn(m4.z, kt_[d + 2], acc[u]);
-        acc[u] = __fmaf_rn(m4.w, kt_[d + 3], acc[u]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (live[u]) a.w.dsc[outo[u]] = __fmul_rn(acc[u], g.c32);
+  for (int i = 0; i < 8; ++i) {
+    const int rr = r0 + tr * 8 + i;
+    if (rr >= nrows) break;
+    const int qb = rr / grp, hq = hk * grp + rr % grp;
+    if (g.causal && kv_tiles_for(qb, s.nq, s.nkv, 1) <= kt) continue;
+    float *dst = a.w.dsc + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * a.L.nkv_pad +
+                 (size_t)kt * kBKV + tk * 8;
+    float4 lo, hi;
+    lo.x = __fmul_rn(acc[i][0], g.c32);
+    lo.y = __fmul_rn(acc[i][1], g.c32);
+    lo.z = __fmul_rn(acc[i][2], g.c32);
+    lo.w = __fmul_rn(acc[i][3], g.c32);
+    hi.x = __fmul_rn(acc[i][4], g.c32);
+    hi.y = __fmul_rn(acc[i][5], g.c32);
+    hi.z = __fmul_rn(acc[i][6], g.c32);
+    hi.w = __fmul_rn(acc[i][7], g.c32);
+    reinterpret_cast<float4 *>(dst)[0] = lo;
+    reinterpret_cast<float4 *>(dst)[1] = hi;
   }
 }
 
@@ -436,18 +490,23 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
   kv_stats_partial<<<dim3(L.nchunk, g.B), threads, 0, st>>>(a);
   kv_stats_final<<<g.B * g.Hkv, g.Dp, 0, st>>>(a);
-  const dim3 kv_grid((g.max_nkv + kBKV - 1) / kBKV, g.Hkv, g.B);
-  const dim3 q_grid((g.max_nq + kBQ - 1) / kBQ, g.Hq, g.B);
+  // every grid dimension at least 1 (a zero-length maximum is legal; the kernels bound-check)
+  const int kv_tiles = max(1, (g.max_nkv + kBKV - 1) / kBKV);
+  const int q_tiles = max(1, (g.max_nq + kBQ - 1) / kBQ);
+  const dim3 kv_grid(kv_tiles, g.Hkv, g.B);
+  const dim3 q_grid(q_tiles, g.Hq, g.B);
+  const int max_rows = (g.Hq / g.Hkv) * q_tiles;
+  const dim3 ds_grid(kv_tiles, (max_rows + kDsRows - 1) / kDsRows, g.B * g.Hkv);
   if (g.Dp == 128) {
     k_quant<128><<<kv_grid, 128, 0, st>>>(a);
     v_quant<128><<<kv_grid, 256, 0, st>>>(a);
     q_quant<128><<<q_grid, 128, 0, st>>>(a);
-    delta_s<128><<<kv_grid, 128, 0, st>>>(a);
+    delta_s<128><<<ds_grid, 256, 0, st>>>(a);
   } else {
     k_quant<64><<<kv_grid, 128, 0, st>>>(a);
     v_quant<64><<<kv_grid, 256, 0, st>>>(a);
     q_quant<64><<<q_grid, 128, 0, st>>>(a);
-    delta_s<64><<<kv_grid, 128, 0, st>>>(a);
+    delta_s<64><<<ds_grid, 256, 0, st>>>(a);
   }
   return cudaGetLastError();
 }
