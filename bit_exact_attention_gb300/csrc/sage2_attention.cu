@@ -1,20 +1,22 @@
 // sage2_attention.cu -- the fused SageAttention2 attention kernel for sm_103a.
 //
 // One CTA per (sequence, q head, 128-row Q tile); ten warps:
-//   warps 0-3  softmax: thread t of warp w owns accumulator row 32w+t (its TMEM lane). Per
-//              128-key tile it loads the whole S row from tensor memory in one instruction,
-//              dequantizes and adds DeltaS with one FMA per element, takes the row maximum,
-//              computes P448 = 2^(S' - m + log2 448) in base 2, writes P~ = e4m3(P448) back to
-//              tensor memory (the A operand of the P~V MMA) and hands alpha = 2^(m_old - m_new)
-//              to the fold warps.
+//   warps 0-3  softmax: thread t of warp w owns accumulator row 32w+t (its TMEM lane). It first
+//              stores its row's Q codes into tensor memory (the A operand of Q K^T). Per 128-key
+//              tile it loads the whole S row in one instruction, dequantizes and adds DeltaS
+//              with one FMA per element, takes the row maximum, computes
+//              P448 = 2^(S' - m + log2 448) in base 2, writes P~ = e4m3(P448) to tensor memory
+//              (the A operand of the P~V MMA) and hands alpha = 2^(m_old - m_new) to the fold.
+//              The arithmetic runs in long independent phases over the 128 values, in place.
 //   warps 4-7  fold + epilogue: thread t of warp 4+w owns row 32w+t of the FP32 output in
 //              registers and folds the fresh per-tile partial: O = alpha O + R. At the end it
 //              divides by the row sum and writes the output row.
-//   warp 8     TMA producer (one lane): Q codes once, then per KV tile the K codes, transposed
-//              V codes, 128 DeltaS*c values and 4 K scales into an ST-stage ring.
-//   warp 9     MMA issuer (one lane) and tensor-memory owner: S = Qcode Kcode^T
-//              (tcgen05 kind::f8f6f4, e4m3 x e4m3 -> f32, both operands from shared memory),
-//              R = P~ Vcode (A from tensor memory), into double-buffered S and R.
+//   warp 8     TMA producer (one lane): per KV tile the K codes, the transposed V codes,
+//              128 DeltaS*c values and 4 K scales into an ST-stage ring.
+//   warp 9     MMA issuer (one lane), tcgen05 kind::f8f6f4 (e4m3 x e4m3 -> f32), A operands from
+//              tensor memory, B from shared memory. Q K^T runs two tiles ahead of the softmax
+//              (S is double-buffered); P~ V runs as soon as every row's P~ is written and the
+//              previous partial is folded.
 // Method (SageAttention2 pages): INT4-grid Q and K codes with per-thread-group scales; P~ and
 // V in e4m3; two-level accumulation of P~V ("SageAttention2: Efficient Attention with Thorough
 // Outlier Smoothing and Per-thread INT4 Quantization" research note, components 2 and 3;
@@ -24,14 +26,13 @@
 // at most 49 and a 128-channel dot product at most 6272 < 2^24, so the FP32 accumulator holds
 // the integer Q K^T exactly.
 //
-// Tensor memory (512 columns): S0 [0,128) S1 [128,256) R0 [256, 256+Dp) R1 [384, 384+Dp);
-// P~ of tile j overwrites the first 32 columns of its S buffer once the softmax has read S.
-//
-// Pipeline per KV tile j (sb = j % 2): the MMA warp issues QK(j+1) as soon as PV(j-1) has
-// finished reading P~(j-1) from S[(j+1)%2], so the tensor core computes the next S while the
-// softmax works on this one; PV(j) waits for P~(j) and for the fold of R(j-2). The alpha of
-// tile j travels through a 4-deep shared ring: the softmax cannot run more than three tiles
-// ahead of the fold (tile j+4 needs PV(j+2), which needs the fold of tile j).
+// Tensor memory (512 columns allocated): S0 [0,128) S1 [128,256) R [256, 256+Dp)
+// P~0 [384,416) P~1 [416,448) Q [448, 448+Dp/4).
+// Ordering: QK(j+2) overwrites S[j%2] once every softmax warp has copied S(j) out (s_free);
+// PV(j) overwrites R once the fold of tile j-1 is done (r_free); the softmax of tile j rewrites
+// P~[j%2] only after PV(j-2) is complete (pv_done). Every barrier is waited on at most one phase
+// behind its next completion, so parity waits cannot alias. The alpha of tile j travels through
+// a 4-deep shared ring: tile j+4 first waits for PV(j+2), which needs the fold of tile j+1.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -43,20 +44,31 @@
 namespace sage2 {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColR0 = 256, kColR1 = 384;
+// Warp roles: 0-3 softmax, 4-7 fold, then the TMA and MMA warps.
+#ifndef SAGE2_TMA_WARP
+#define SAGE2_TMA_WARP 8
+#endif
+#ifndef SAGE2_MMA_WARP
+#define SAGE2_MMA_WARP 9
+#endif
+constexpr int kTmaWarp = SAGE2_TMA_WARP, kMmaWarp = SAGE2_MMA_WARP;
+constexpr int kThreads = 32 * ((kTmaWarp > kMmaWarp ? kTmaWarp : kMmaWarp) + 1);
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColR = 256, kColP0 = 384, kColP1 = 416,
+                   kColQ = 448;
 constexpr uint32_t kTmemCols = 512;
 
 // wait-site ids reported in the status word
 enum : int {
   kSiteQ = 1, kSiteKvFull = 2, kSiteKvEmpty = 3, kSiteSFull = 4, kSitePFull = 5, kSiteRFull = 6,
-  kSiteRFree = 7, kSiteKvFullSm = 8, kSiteAFull = 9, kSiteLFull = 10
+  kSiteRFree = 7, kSiteKvFullSm = 8, kSiteAFull = 9, kSiteLFull = 10, kSiteSFree = 11,
+  kSitePvDone = 12
 };
 
 struct AttnArgs {
   Geometry g;
   Layout L;
   const float *qscale, *kscale, *dsc, *vscale;
+  const uint8_t *qcode;
   void *out;
   int out_dtype;
   int *status;
@@ -65,16 +77,15 @@ struct AttnArgs {
 
 template <int DP, int ST>
 struct SmemPlan {
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + 128 * DP;
+  static constexpr int kK = 0;
   static constexpr int kV = kK + ST * 128 * DP;
   static constexpr int kDsc = kV + ST * DP * 128;
   static constexpr int kSk = kDsc + ST * 512;
   static constexpr int kAlpha = kSk + ST * 16;         // float [4][128]
   static constexpr int kLsum = kAlpha + 4 * 128 * 4;  // float [128]
   static constexpr int kBar = kLsum + 128 * 4;
-  // q, full[ST], empty[ST], s[2], p[2], r_full[2], r_free[2], a[4], l, drain
-  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 2 + 2 + 4 + 1 + 1;
+  // q, full[ST], empty[ST], s_full[2], s_free[2], p[2], pv_done[2], r_free, a[4], l, drain
+  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 2 + 2 + 1 + 4 + 1 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
@@ -90,8 +101,8 @@ __device__ bool drain_wait(uint64_t *bar, uint32_t parity) {
 
 template <int DP, int ST, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-             const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+    attn_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+             const AttnArgs a) {
   using P = SmemPlan<DP, ST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -128,45 +139,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  uint8_t *sQ = smem + P::kQ;
   float *alpha_ring = reinterpret_cast<float *>(smem + P::kAlpha);
   float *lsum = reinterpret_cast<float *>(smem + P::kLsum);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::kBar);
   uint64_t *q_full = bars;
   uint64_t *kv_full = bars + 1;
   uint64_t *kv_empty = kv_full + ST;
-  uint64_t *s_full = kv_empty + ST;
-  uint64_t *p_full = s_full + 2;
-  uint64_t *r_full = p_full + 2;
-  uint64_t *r_free = r_full + 2;
-  uint64_t *a_full = r_free + 2;
+  uint64_t *s_full = kv_empty + ST;  // [2]
+  uint64_t *s_free = s_full + 2;     // [2]
+  uint64_t *p_full = s_free + 2;     // [2]
+  uint64_t *pv_done = p_full + 2;    // [2]
+  uint64_t *r_free = pv_done + 2;
+  uint64_t *a_full = r_free + 1;     // [4]
   uint64_t *l_full = a_full + 4;
   uint64_t *drain = l_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kMisc + 4);
 
-  if (warp == 8 && lane == 0) {
-    mbar_init(q_full, 1);
+  if (warp == kTmaWarp && lane == 0) {
+    mbar_init(q_full, 4);
     for (int i = 0; i < ST; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
       mbar_init(&p_full[i], 4);
-      mbar_init(&r_full[i], 1);
-      mbar_init(&r_free[i], 4);
+      mbar_init(&pv_done[i], 1);
     }
+    mbar_init(r_free, 4);
     for (int i = 0; i < 4; ++i) mbar_init(&a_full[i], 4);
     mbar_init(l_full, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -176,87 +187,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
   const AbortCtx ab{abort_flag, a.status};
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer (one lane)
     if (lane == 0) {
-      const int yq = hq * a.L.Tq + s.qpad0 + qt * kBQ;
       const int yk0 = hk * a.L.Tkv + s.kvpad0;
-      const int yv = hk * DP;
       const float *dsc_row =
           a.dsc + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qt) * a.L.nkv_pad;
       const float *sk_row = a.kscale + (size_t)hk * (a.L.Tkv / kGK) + s.kvpad0 / kGK;
       const bool skip = DBG && a.dbg.skip_loads;
-      bool q_issued = false;
       int issued = 0;
-      if (!skip) {
-        mbar_arrive_expect_tx(q_full, 128 * DP);
-        tma_load_2d(sQ, &tm_q, 0, yq, q_full);
-        q_issued = true;
-      }
       for (int j = 0; j < T; ++j) {
         const int st = j % ST;
-        if (j >= ST && !mbar_wait(&kv_empty[st], ((j / ST) - 1) & 1, ab, kSiteKvEmpty)) break;
+        if (j >= ST && !mbar_wait<true>(&kv_empty[st], ((j / ST) - 1) & 1, ab, kSiteKvEmpty)) break;
         if (skip) continue;
-        uint8_t *sK = smem + P::kK + st * 128 * DP;
-        uint8_t *sV = smem + P::kV + st * DP * 128;
-        float *sD = reinterpret_cast<float *>(smem + P::kDsc + st * 512);
-        float *sS = reinterpret_cast<float *>(smem + P::kSk + st * 16);
         mbar_arrive_expect_tx(&kv_full[st], 128 * DP + DP * 128 + 512 + 16);
-        tma_load_2d(sK, &tm_k, 0, yk0 + j * kBKV, &kv_full[st]);
-        tma_load_2d(sV, &tm_v, s.kvpad0 + j * kBKV, yv, &kv_full[st]);
-        bulk_load(sD, dsc_row + (size_t)j * kBKV, 512, &kv_full[st]);
-        bulk_load(sS, sk_row + j * (kBKV / kGK), 16, &kv_full[st]);
+        tma_load_2d(smem + P::kK + st * 128 * DP, &tm_k, 0, yk0 + j * kBKV, &kv_full[st]);
+        tma_load_2d(smem + P::kV + st * DP * 128, &tm_v, s.kvpad0 + j * kBKV, hk * DP,
+                    &kv_full[st]);
+        bulk_load(smem + P::kDsc + st * 512, dsc_row + (size_t)j * kBKV, 512, &kv_full[st]);
+        bulk_load(smem + P::kSk + st * 16, sk_row + j * (kBKV / kGK), 16, &kv_full[st]);
         issued = j + 1;
       }
       if (*abort_flag) {  // let the copies already issued land before the CTA exits
-        if (q_issued) drain_wait(q_full, 0);
         for (int n = issued > ST ? issued - ST : 0; n < issued; ++n)
           drain_wait(&kv_full[n % ST], (n / ST) & 1);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (one lane)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
-      const uint64_t qdesc = sdesc_kmajor(smem_u32(sQ), DP);
-      bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
-      auto issue_qk = [&](int j) {
-        const int st = j % ST;
-        const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + st * 128 * DP), DP);
+      auto issue_qk = [&](int j) {  // S[j % 2] = Qcode Kcode(j)^T, A from tensor memory
+        const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + (j % ST) * 128 * DP), DP);
         const uint32_t dS = tbase + ((j & 1) ? kColS1 : kColS0);
 #pragma unroll
         for (int kk = 0; kk < DP / 32; ++kk)
-          mma_e4m3_ss(dS, qdesc + (uint64_t)(kk * 2), kdesc + (uint64_t)(kk * 2), idesc_qk, kk > 0);
+          mma_e4m3_ts(dS, tbase + kColQ + kk * 8, kdesc + (uint64_t)(kk * 2), idesc_qk, kk > 0);
         mma_commit(&s_full[j & 1]);
       };
-      if (ok) ok = mbar_wait(&kv_full[0], 0, ab, kSiteKvFull);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0);
+      bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
+      for (int j = 0; ok && j < 2 && j < T; ++j) {  // the first two tiles' Q K^T
+        ok = mbar_wait(&kv_full[j], 0, ab, kSiteKvFull);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(j);
+        }
       }
       for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T) {
-          ok = mbar_wait(&kv_full[(j + 1) % ST], ((j + 1) / ST) & 1, ab, kSiteKvFull);
-          // S[(j+1)%2] still holds P~(j-1): PV(j-1) must have finished reading it
-          if (ok && j >= 1) ok = mbar_wait(&r_full[(j - 1) & 1], ((j - 1) >> 1) & 1, ab, kSiteRFull);
+        const int sb = j & 1;
+        // Q K^T two tiles ahead, into the S buffer the softmax of tile j has just copied out
+        if (j + 2 < T) {
+          ok = mbar_wait(&s_free[sb], (j >> 1) & 1, ab, kSiteSFree) &&
+               mbar_wait(&kv_full[(j + 2) % ST], ((j + 2) / ST) & 1, ab, kSiteKvFull);
           if (!ok) break;
           tc_fence_after();
-          issue_qk(j + 1);
+          issue_qk(j + 2);
         }
-        ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, ab, kSitePFull);
-        if (ok && j >= 2) ok = mbar_wait(&r_free[j & 1], ((j - 2) >> 1) & 1, ab, kSiteRFree);
+        // P~(j) V(j) once every row's P~ is written and R is folded
+        ok = mbar_wait(&p_full[sb], (j >> 1) & 1, ab, kSitePFull);
+        if (ok && j >= 1) ok = mbar_wait(r_free, (j - 1) & 1, ab, kSiteRFree);
         if (!ok) break;
         tc_fence_after();
-        const int st = j % ST;
-        const uint64_t vdesc = sdesc_kmajor(smem_u32(smem + P::kV + st * DP * 128), 128);
-        const uint32_t aP = tbase + ((j & 1) ? kColS1 : kColS0);
-        const uint32_t dR = tbase + ((j & 1) ? kColR1 : kColR0);
+        const uint64_t vdesc = sdesc_kmajor(smem_u32(smem + P::kV + (j % ST) * DP * 128), 128);
+        const uint32_t aP = tbase + (sb ? kColP1 : kColP0);
 #pragma unroll
         for (int kk = 0; kk < kBKV / 32; ++kk)
-          mma_e4m3_ts(dR, aP + kk * 8, vdesc + (uint64_t)(kk * 2), idesc_pv, kk > 0);
-        mma_commit(&r_full[j & 1]);
-        mma_commit(&kv_empty[st]);
+          mma_e4m3_ts(tbase + kColR, aP + kk * 8, vdesc + (uint64_t)(kk * 2), idesc_pv, kk > 0);
+        mma_commit(&pv_done[sb]);
+        mma_commit(&kv_empty[j % ST]);
       }
       mma_commit(drain);  // every MMA issued above completes before tensor memory is freed
       drain_wait(drain, 0);
@@ -272,25 +271,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int last_key = g.causal ? min(i + (s.nkv - s.nq), s.nkv - 1) : s.nkv - 1;
     const float L32 = 8.8073549220576041f;  // fl32(log2(448))
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    {  // this row's Q codes (Dp bytes) into tensor memory: the A operand of Q K^T
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(
+          a.qcode + ((size_t)hq * a.L.Tq + s.qpad0 + qt * kBQ + row) * DP);
+      uint32_t qw[DP / 4];
+#pragma unroll
+      for (int c = 0; c < DP / 16; ++c) {
+        const uint4 u = __ldg(qrow + c);
+        qw[4 * c] = u.x;
+        qw[4 * c + 1] = u.y;
+        qw[4 * c + 2] = u.z;
+        qw[4 * c + 3] = u.w;
+      }
+#pragma unroll
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t w8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w8[e] = qw[8 * c + e];
+        tmem_st8(tbase + lane_base + kColQ + 8 * c, w8);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    }
+    // Every decision to continue is warp-uniform: after each wait the warp takes lane 0's result.
+    bool ok = true;
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < T; ++j) {
+    for (int j = 0; ok && j < T; ++j) {
       const int sb = j & 1, st = j % ST;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, ab, kSiteSFull)) break;
-      if (!mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm)) break;
+      // S(j) computed, its ring stage loaded, and P~[sb] no longer read by PV(j-2)
+      ok = mbar_wait(&s_full[sb], (j >> 1) & 1, ab, kSiteSFull) &&
+           mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm) &&
+           (j < 2 || mbar_wait(&pv_done[sb], ((j - 2) >> 1) & 1, ab, kSitePvDone));
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
       tc_fence_after();
-      const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 512);
-      const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
-      const int lim = last_key - j * kBKV;  // columns 0..lim are visible to this row
       const uint32_t tS = tbase + lane_base + (sb ? kColS1 : kColS0);
+      const uint32_t tP = tbase + lane_base + (sb ? kColP1 : kColP0);
       uint32_t v[128];
       tmem_ld128(tS, v);
+      // S(j) is in registers: the MMA warp may compute S(j+2) into this buffer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
       if (DBG && j == a.dbg.kt) {
 #pragma unroll
         for (int e = 0; e < 128; ++e) a.dbg.s_out[row * 128 + e] = __uint_as_float(v[e]);
       }
+      const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 512);
+      const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
+      const int lim = last_key - j * kBKV;  // columns 0..lim are visible to this row
+      // The arithmetic below runs in long independent phases over the 128 values, in place,
+      // so the scheduler can keep the FMA and MUFU pipes busy with one warp.
       float x[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; ++c) {  // S' = A * (s_q c s_k) + DeltaS c
         const float mult = __fmul_rn(sqc, skv[c]);
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -306,34 +342,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 128; ++e) x[e] = (e <= lim) ? x[e] : -INFINITY;
       }
-      float mx = m;
+      // row maximum: eight independent 3-input max chains, then a small tree
+      float mk[8];
 #pragma unroll
-      for (int e = 0; e < 128; e += 2) mx = max3(mx, x[e], x[e + 1]);
-      const float m_new = mx;
+      for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[16 * k], x[16 * k + 1]);
+#pragma unroll
+      for (int e = 2; e < 16; e += 2)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = max3(mk[k], x[16 * k + e], x[16 * k + e + 1]);
+      const float m_new = max3(max3(mk[0], mk[1], mk[2]), max3(mk[3], mk[4], mk[5]),
+                               max3(mk[6], mk[7], m));
       const float m448 = (m_new == -INFINITY) ? 0.f : __fsub_rn(m_new, L32);
       const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(__fsub_rn(m, m_new));
       // P448 = 2^(S' - m448); masked keys have S' = -inf and give 0
-      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 keys -> 8 words of P~ per chunk
-        uint32_t pk[8];
+      for (int e = 0; e < 128; e += 2) add2(x[e], x[e + 1], x[e], x[e + 1], -m448, -m448);
 #pragma unroll
-        for (int e = c * 32; e < c * 32 + 32; e += 4) {
-          float t0, t1, t2, t3;
-          add2(t0, t1, x[e], x[e + 1], -m448, -m448);
-          add2(t2, t3, x[e + 2], x[e + 3], -m448, -m448);
-          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1), p2 = ex2_approx(t2),
-                      p3 = ex2_approx(t3);
-          add2(ps0, ps1, ps0, ps1, p0, p1);
-          add2(ps0, ps1, ps0, ps1, p2, p3);
-          pk[(e - c * 32) / 4] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
-        }
-        tmem_st8(tS + c * 8, pk);
-        if (DBG && j == a.dbg.kt) {
+      for (int e = 0; e < 128; ++e) x[e] = ex2_approx(x[e]);
+      float ps[8][2];  // row sum: eight independent packed accumulators
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<uint32_t *>(a.dbg.p_out + row * 128 + c * 32 + e * 4) = pk[e];
-        }
+      for (int k = 0; k < 8; ++k) ps[k][0] = ps[k][1] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 128; e += 2)
+        add2(ps[(e >> 1) & 7][0], ps[(e >> 1) & 7][1], ps[(e >> 1) & 7][0], ps[(e >> 1) & 7][1],
+             x[e], x[e + 1]);
+      uint32_t pk[32];  // P~ = e4m3(P448), four keys per word
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        pk[e] = cvt_e4m3x2(x[4 * e], x[4 * e + 1]) | (cvt_e4m3x2(x[4 * e + 2], x[4 * e + 3]) << 16);
+      tmem_st32(tP, pk);
+      if (DBG && j == a.dbg.kt) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          *reinterpret_cast<uint32_t *>(a.dbg.p_out + row * 128 + e * 4) = pk[e];
       }
       tmem_st_wait();
       tc_fence_before();
@@ -343,13 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&p_full[sb]);
         mbar_arrive(&a_full[j & 3]);
       }
-      l = __fmaf_rn(alpha, l, __fadd_rn(ps0, ps1));
+      float psum[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        psum[k] = __fadd_rn(__fadd_rn(ps[2 * k][0], ps[2 * k][1]), __fadd_rn(ps[2 * k + 1][0], ps[2 * k + 1][1]));
+      l = __fmaf_rn(alpha, l, __fadd_rn(__fadd_rn(psum[0], psum[1]), __fadd_rn(psum[2], psum[3])));
       m = m_new;
     }
     lsum[row] = l;
     __syncwarp();
     if (lane == 0) mbar_arrive(l_full);
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ fold + epilogue (warps 4-7)
     const int q4 = warp - 4;
     const int row = q4 * 32 + lane;
@@ -361,14 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int d = 0; d < DP; ++d) O[d] = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      const int sb = j & 1;
       ok = mbar_wait(&a_full[j & 3], (j >> 2) & 1, ab, kSiteAFull);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const float alpha = alpha_ring[(j & 3) * 128 + row];
-      ok = mbar_wait(&r_full[sb], (j >> 1) & 1, ab, kSiteRFull);
+      ok = mbar_wait(&pv_done[j & 1], (j >> 1) & 1, ab, kSiteRFull);  // R(j) is complete
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tR = tbase + lane_base + (sb ? kColR1 : kColR0);
+      const uint32_t tR = tbase + lane_base + kColR;
 #pragma unroll
       for (int c = 0; c < DP / 16; ++c) {
         uint32_t v[16];
@@ -384,9 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&r_free[sb]);
+      if (lane == 0) mbar_arrive(r_free);
     }
     if (ok) ok = mbar_wait(l_full, 0, ab, kSiteLFull);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     // ------------------------------------------------------------ epilogue
     if (ok && row_ok && !*abort_flag) {
       const float l = lsum[row];
@@ -430,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tbase, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tbase, kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
@@ -468,8 +515,8 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, u
 }
 
 template <int DP, int ST, bool DBG>
-cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                     const AttnArgs &a, dim3 grid, cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, dim3 grid,
+                     cudaStream_t st) {
   using P = SmemPlan<DP, ST>;
   // at least 116 KB so that a single CTA occupies an SM (each allocates all 512 TMEM columns)
   constexpr int kSmem = P::kBytes > 116 * 1024 ? P::kBytes : 116 * 1024;
@@ -480,7 +527,7 @@ cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attn_fwd<DP, ST, DBG><<<grid, kThreads, kSmem, st>>>(mq, mk, mv, a);
+  attn_fwd<DP, ST, DBG><<<grid, kThreads, kSmem, st>>>(mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -496,26 +543,26 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
   a.kscale = w.kscale;
   a.dsc = w.dsc;
   a.vscale = w.vscale;
+  a.qcode = w.qcode;
   a.out = out;
   a.out_dtype = out_dtype;
   a.status = w.status;
   a.dbg = dbg ? *dbg : AttnDebug{0, 0, 0, 0, nullptr, nullptr, nullptr, 0};
   const CUtensorMapSwizzle qk_sw =
       g.Dp == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, w.qcode, g.Dp, (uint64_t)g.Hq * L.Tq, g.Dp, 128, qk_sw) ||
-      !make_map(&mk, w.kcode, g.Dp, (uint64_t)g.Hkv * L.Tkv, g.Dp, 128, qk_sw) ||
+  CUtensorMap mk, mv;
+  if (!make_map(&mk, w.kcode, g.Dp, (uint64_t)g.Hkv * L.Tkv, g.Dp, 128, qk_sw) ||
       !make_map(&mv, w.vcodeT, L.Tkv, (uint64_t)g.Hkv * g.Dp, 128, g.Dp,
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int nqt = (g.max_nq + kBQ - 1) / kBQ;
   if (dbg) {
-    if (g.Dp == 128) return launch_t<128, 3, true>(mq, mk, mv, a, dim3(1), st);
-    return launch_t<64, 4, true>(mq, mk, mv, a, dim3(1), st);
+    if (g.Dp == 128) return launch_t<128, 6, true>(mk, mv, a, dim3(1), st);
+    return launch_t<64, 8, true>(mk, mv, a, dim3(1), st);
   }
   const dim3 grid(nqt, g.Hq, g.B);
-  if (g.Dp == 128) return launch_t<128, 3, false>(mq, mk, mv, a, grid, st);
-  return launch_t<64, 4, false>(mq, mk, mv, a, grid, st);
+  if (g.Dp == 128) return launch_t<128, 6, false>(mk, mv, a, grid, st);
+  return launch_t<64, 8, false>(mk, mv, a, grid, st);
 }
 
 }  // namespace sage2

@@ -61,20 +61,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same test with a suspend-time hint: a thread whose phase is not complete sleeps (up to
+// `ns` nanoseconds, or until the phase completes) instead of retrying at once, which leaves the
+// shared-memory instruction path to the other warps of its sub-partition. Wake-up is slower, so
+// this suits waiters with slack.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Per-CTA abort state: a shared flag plus the global status word.
 struct AbortCtx {
   volatile int *flag;  // shared memory
   int *status;         // global memory (may be null)
 };
 
-// Wait until the phase of `bar` with parity `parity` has completed. Returns false if the
-// wait gave up (time limit) or another warp already gave up.
-static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortCtx ab, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+#ifndef SAGE2_LAZY_NS
+#define SAGE2_LAZY_NS 1000u
+#endif
+
+// Slow path of mbar_wait: keep trying until the phase completes, another warp of the CTA gave
+// up, or SAGE2_WAIT_NS of global time passed. Lazy waiters sleep between tries.
+template <bool LAZY>
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, AbortCtx ab,
+                                                   int site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
+    if (LAZY ? mbar_try_wait_sleep(bar, parity, SAGE2_LAZY_NS) : mbar_try_wait(bar, parity))
+      return true;
+    if (LAZY || (it & 31u) == 0) {
       if (*ab.flag) return false;
       if (global_timer_ns() - t0 > SAGE2_WAIT_NS) {
         *ab.flag = 1;
@@ -83,6 +105,14 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Ab
       }
     }
   }
+}
+
+// Wait until the phase of `bar` with parity `parity` has completed. Returns false if the
+// wait gave up (time limit) or another warp already gave up. The first try is inline.
+template <bool LAZY = false>
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortCtx ab, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow<LAZY>(bar, parity, ab, site);
 }
 
 // ------------------------------------------------------------------ TMA / bulk copies
