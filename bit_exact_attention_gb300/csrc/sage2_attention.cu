@@ -1,22 +1,26 @@
 // sage2_attention.cu -- the fused SageAttention2 attention kernel for sm_103a.
 //
-// One CTA per (sequence, q head, 128-row Q tile); ten warps:
-//   warps 0-3  softmax: thread t of warp w owns accumulator row 32w+t (its TMEM lane). It first
-//              stores its row's Q codes into tensor memory (the A operand of Q K^T). Per 128-key
-//              tile it loads the whole S row in one instruction, dequantizes and adds DeltaS
-//              with one FMA per element, takes the row maximum, computes
-//              P448 = 2^(S' - m + log2 448) in base 2, writes P~ = e4m3(P448) to tensor memory
-//              (the A operand of the P~V MMA) and hands alpha = 2^(m_old - m_new) to the fold.
-//              The arithmetic runs in long independent phases over the 128 values, in place.
-//   warps 4-7  fold + epilogue: thread t of warp 4+w owns row 32w+t of the FP32 output in
-//              registers and folds the fresh per-tile partial: O = alpha O + R. At the end it
-//              divides by the row sum and writes the output row.
-//   warp 8     TMA producer (one lane): per KV tile the K codes, the transposed V codes,
-//              128 DeltaS*c values and 4 K scales into an ST-stage ring.
-//   warp 9     MMA issuer (one lane), tcgen05 kind::f8f6f4 (e4m3 x e4m3 -> f32), A operands from
-//              tensor memory, B from shared memory. Q K^T runs two tiles ahead of the softmax
-//              (S is double-buffered); P~ V runs as soon as every row's P~ is written and the
-//              previous partial is folded.
+// One CTA per (sequence, q head, 128-row Q tile); twelve warps in three warpgroups:
+//   warp 0      TMA producer (one lane): per KV tile the K codes, the transposed V codes,
+//               128 DeltaS*c values and 4 K scales into an ST-stage ring.
+//   warps 1, 2  MMA issuers (one lane each), tcgen05 kind::f8f6f4 (e4m3 x e4m3 -> f32), A from
+//               tensor memory, B from shared memory: warp 1 issues S(j) = Qcode Kcode(j)^T as
+//               soon as S is free, warp 2 issues R(j) = P~(j) V(j) into R[j%2] as soon as P~(j)
+//               is written, so neither stream waits behind the other.
+//   warp 3      idle (it only gives its registers away).
+//   warps 4-7   softmax: thread t of warp 4+w owns accumulator row 32w+t (its TMEM lane). It
+//               first stores its row's Q codes into tensor memory (the A operand of Q K^T).
+//               Per 128-key tile it loads the S row into registers (freeing S for the next
+//               Q K^T at once), dequantizes and adds DeltaS with one FMA per element, takes the
+//               row maximum, computes P448 = 2^(S' - m + log2 448) in base 2, writes
+//               P~ = e4m3(P448) into tensor memory (the A operand of the P~V MMA) and hands
+//               alpha = 2^(m_old - m_new) to the fold. The load of S(j) is issued before the
+//               other waits of tile j, and P~(j-1) is handed over after it, so their latencies
+//               overlap.
+//   warps 8-11  fold + epilogue: thread t of warp 8+w owns row 32w+t of the FP32 output in
+//               registers and folds each fresh per-tile partial: O = alpha O + R. At the end it
+//               divides by the row sum and writes the output row.
+// setmaxnreg moves registers from the control warpgroup to the softmax and fold warpgroups.
 // Method (SageAttention2 pages): INT4-grid Q and K codes with per-thread-group scales; P~ and
 // V in e4m3; two-level accumulation of P~V ("SageAttention2: Efficient Attention with Thorough
 // Outlier Smoothing and Per-thread INT4 Quantization" research note, components 2 and 3;
@@ -26,13 +30,14 @@
 // at most 49 and a 128-channel dot product at most 6272 < 2^24, so the FP32 accumulator holds
 // the integer Q K^T exactly.
 //
-// Tensor memory (512 columns allocated): S0 [0,128) S1 [128,256) R [256, 256+Dp)
+// Tensor memory (512 columns allocated): S [0,128) R0 [128, 128+Dp) R1 [256, 256+Dp)
 // P~0 [384,416) P~1 [416,448) Q [448, 448+Dp/4).
-// Ordering: QK(j+2) overwrites S[j%2] once every softmax warp has copied S(j) out (s_free);
-// PV(j) overwrites R once the fold of tile j-1 is done (r_free); the softmax of tile j rewrites
-// P~[j%2] only after PV(j-2) is complete (pv_done). Every barrier is waited on at most one phase
-// behind its next completion, so parity waits cannot alias. The alpha of tile j travels through
-// a 4-deep shared ring: tile j+4 first waits for PV(j+2), which needs the fold of tile j+1.
+// Ordering: QK(j+1) overwrites S once the softmax has read S(j) (s_free); PV(j) overwrites
+// R[j%2] once the fold of tile j-2 has read it (r_free[j%2]); the softmax of tile j rewrites
+// P~[j%2] only after PV(j-2) is complete (pv_done[j%2]). Every mbarrier is waited on at most
+// one phase behind its next completion, so parity waits cannot alias. The alpha of tile j
+// travels through a 4-deep shared ring; tile j+4 writes its slot only after PV(j+2), which needs
+// the fold of tile j.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -44,16 +49,19 @@
 namespace sage2 {
 namespace {
 
-// Warp roles: 0-3 softmax, 4-7 fold, then the TMA and MMA warps.
-#ifndef SAGE2_TMA_WARP
-#define SAGE2_TMA_WARP 8
-#endif
-#ifndef SAGE2_MMA_WARP
-#define SAGE2_MMA_WARP 9
-#endif
-constexpr int kTmaWarp = SAGE2_TMA_WARP, kMmaWarp = SAGE2_MMA_WARP;
-constexpr int kThreads = 32 * ((kTmaWarp > kMmaWarp ? kTmaWarp : kMmaWarp) + 1);
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColR = 256, kColP0 = 384, kColP1 = 416,
+constexpr int kTmaWarp = 0, kMmaWarp = 1, kPvWarp = 2, kSmWarp0 = 4, kFoldWarp0 = 8;
+constexpr int kNumWarps = 12, kThreads = 32 * kNumWarps;
+// Registers per thread after the split (the launch gives every warpgroup 128; setmaxnreg.inc
+// waits until the other warpgroups have released enough, so the sum must stay within 4 x 128).
+constexpr int kRegsLaunch = 168;  // 65536 registers / 384 threads, in steps of 8
+constexpr int kRegsCtl = 40, kRegsSoftmax = 232, kRegsFold = 200;
+static_assert(kRegsCtl + kRegsSoftmax + kRegsFold <= 3 * kRegsLaunch,
+              "register split above the launch budget");
+// setmaxnreg.dec may only lower and setmaxnreg.inc only raise the current count
+static_assert(kRegsCtl <= kRegsLaunch, "the control warpgroup releases");
+static_assert(kRegsSoftmax >= kRegsLaunch && kRegsFold >= kRegsLaunch,
+              "the softmax and fold warpgroups acquire");
+constexpr uint32_t kColS = 0, kColR0 = 128, kColR1 = 256, kColP0 = 384, kColP1 = 416,
                    kColQ = 448;
 constexpr uint32_t kTmemCols = 512;
 
@@ -77,26 +85,72 @@ struct AttnArgs {
 
 template <int DP, int ST>
 struct SmemPlan {
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + ST * 128 * DP;
-  static constexpr int kDsc = kV + ST * DP * 128;
-  static constexpr int kSk = kDsc + ST * 512;
-  static constexpr int kAlpha = kSk + ST * 16;         // float [4][128]
-  static constexpr int kLsum = kAlpha + 4 * 128 * 4;  // float [128]
+  static constexpr int kK = 0;                           // [ST][128 keys][DP]     (swizzled)
+  static constexpr int kV = kK + ST * 128 * DP;          // [ST][DP][128 keys]     (swizzled)
+  static constexpr int kDsc = kV + ST * DP * 128;        // float [ST][128]
+  static constexpr int kSk = kDsc + ST * 512;            // float [ST][4]
+  static constexpr int kAlpha = kSk + ST * 16;           // float [4][128]
+  static constexpr int kLsum = kAlpha + 4 * 128 * 4;     // float [128]
   static constexpr int kBar = kLsum + 128 * 4;
-  // q, full[ST], empty[ST], s_full[2], s_free[2], p[2], pv_done[2], r_free, a[4], l, drain
-  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 2 + 2 + 1 + 4 + 1 + 1;
+  // q, full[ST], empty[ST], s_full, s_free, p_full[2], pv_done[2], r_free[2], a[4], l, drain[2]
+  static constexpr int kNumBars = 1 + 2 * ST + 1 + 1 + 2 + 2 + 2 + 4 + 1 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
+  static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
 
 // Waits that ignore the abort flag (used to drain copies and MMAs already in flight).
-__device__ bool drain_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > SAGE2_WAIT_NS) return false;
   return true;
+}
+
+__device__ __forceinline__ bool warp_all(bool ok) {
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// S' = A * (s_q c s_k) + DeltaS c for 64 keys (one FMA each), masked beyond `lim`, and their max.
+__device__ __forceinline__ float logits64(float (&x)[64], const uint32_t (&v)[64], const float *dsc,
+                                          const float *skv, float sqc, int lim) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const float mult = __fmul_rn(sqc, skv[c]);
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 d4 = *reinterpret_cast<const float4 *>(dsc + c * 32 + e);
+      const int k0 = c * 32 + e;
+      fma2(x[k0], x[k0 + 1], __uint_as_float(v[k0]), __uint_as_float(v[k0 + 1]), mult, mult, d4.x,
+           d4.y);
+      fma2(x[k0 + 2], x[k0 + 3], __uint_as_float(v[k0 + 2]), __uint_as_float(v[k0 + 3]), mult,
+           mult, d4.z, d4.w);
+    }
+  }
+  if (lim < 63) {  // diagonal / ragged tile: keys beyond lim are not visible
+#pragma unroll
+    for (int e = 0; e < 64; ++e) x[e] = (e <= lim) ? x[e] : -INFINITY;
+  }
+  float mk[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) mk[k] = fmaxf(x[16 * k], x[16 * k + 1]);
+#pragma unroll
+  for (int e = 2; e < 16; e += 2)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mk[k] = max3(mk[k], x[16 * k + e], x[16 * k + e + 1]);
+  return max3(mk[0], mk[1], fmaxf(mk[2], mk[3]));
+}
+
+// End of every role branch: all 512 threads meet once more (each warp from its own branch, so
+// the per-warpgroup register budgets never merge into one code path), then the MMA warp frees
+// tensor memory.
+__device__ __forceinline__ void cta_teardown(bool owner, uint32_t tbase) {
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (owner) tmem_dealloc(tbase, kTmemCols);
 }
 
 template <int DP, int ST, bool DBG>
@@ -145,14 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *q_full = bars;
   uint64_t *kv_full = bars + 1;
   uint64_t *kv_empty = kv_full + ST;
-  uint64_t *s_full = kv_empty + ST;  // [2]
-  uint64_t *s_free = s_full + 2;     // [2]
-  uint64_t *p_full = s_free + 2;     // [2]
+  uint64_t *s_full = kv_empty + ST;  // completed by QK(j), once per tile
+  uint64_t *s_free = s_full + 1;     // completed when the softmax has read S(j)
+  uint64_t *p_full = s_free + 1;     // [2]
   uint64_t *pv_done = p_full + 2;    // [2]
-  uint64_t *r_free = pv_done + 2;
-  uint64_t *a_full = r_free + 1;     // [4]
+  uint64_t *r_free = pv_done + 2;    // [2]
+  uint64_t *a_full = r_free + 2;     // [4]
   uint64_t *l_full = a_full + 4;
-  uint64_t *drain = l_full + 1;
+  uint64_t *drain = l_full + 1;     // [2]: one per MMA-issuing warp
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kMisc + 4);
 
@@ -162,16 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
+    mbar_init(s_free, 4);
+    mbar_init(s_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&r_free[i], 4);
     }
-    mbar_init(r_free, 4);
     for (int i = 0; i < 4; ++i) mbar_init(&a_full[i], 4);
     mbar_init(l_full, 4);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_k);
@@ -187,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
   const AbortCtx ab{abort_flag, a.status};
 
-  if (warp == kTmaWarp) {
+  if (warp < 4) {
+    regs_release<kRegsCtl>();
+    if (warp == kTmaWarp && lane == 0) {
     // ------------------------------------------------------------ TMA producer (one lane)
-    if (lane == 0) {
       const int yk0 = hk * a.L.Tkv + s.kvpad0;
       const float *dsc_row =
           a.dsc + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qt) * a.L.nkv_pad;
@@ -212,57 +268,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = issued > ST ? issued - ST : 0; n < issued; ++n)
           drain_wait(&kv_full[n % ST], (n / ST) & 1);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer (one lane)
-    if (lane == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
+    // ------------------------------------------------------------ Q K^T issuer (one lane)
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
-      constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
-      auto issue_qk = [&](int j) {  // S[j % 2] = Qcode Kcode(j)^T, A from tensor memory
-        const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + (j % ST) * 128 * DP), DP);
-        const uint32_t dS = tbase + ((j & 1) ? kColS1 : kColS0);
-#pragma unroll
-        for (int kk = 0; kk < DP / 32; ++kk)
-          mma_e4m3_ts(dS, tbase + kColQ + kk * 8, kdesc + (uint64_t)(kk * 2), idesc_qk, kk > 0);
-        mma_commit(&s_full[j & 1]);
-      };
       bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
-      for (int j = 0; ok && j < 2 && j < T; ++j) {  // the first two tiles' Q K^T
-        ok = mbar_wait(&kv_full[j], 0, ab, kSiteKvFull);
-        if (ok) {
-          tc_fence_after();
-          issue_qk(j);
-        }
-      }
       for (int j = 0; ok && j < T; ++j) {
-        const int sb = j & 1;
-        // Q K^T two tiles ahead, into the S buffer the softmax of tile j has just copied out
-        if (j + 2 < T) {
-          ok = mbar_wait(&s_free[sb], (j >> 1) & 1, ab, kSiteSFree) &&
-               mbar_wait(&kv_full[(j + 2) % ST], ((j + 2) / ST) & 1, ab, kSiteKvFull);
-          if (!ok) break;
-          tc_fence_after();
-          issue_qk(j + 2);
-        }
-        // P~(j) V(j) once every row's P~ is written and R is folded
-        ok = mbar_wait(&p_full[sb], (j >> 1) & 1, ab, kSitePFull);
-        if (ok && j >= 1) ok = mbar_wait(r_free, (j - 1) & 1, ab, kSiteRFree);
+        // S is free once the four warps of tile j-1 have read it
+        ok = (j == 0 || mbar_wait<true>(s_free, (j - 1) & 1, ab, kSiteSFree)) &&
+             mbar_wait<true>(&kv_full[j % ST], (j / ST) & 1, ab, kSiteKvFull);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + (j % ST) * 128 * DP), DP);
+#pragma unroll
+        for (int kk = 0; kk < DP / 32; ++kk)  // A = the Q codes in tensor memory
+          mma_e4m3_ts(tbase + kColS, tbase + kColQ + kk * 8, kdesc + (uint64_t)(kk * 2), idesc_qk,
+                      kk > 0);
+        mma_commit(s_full);
+      }
+      mma_commit(&drain[0]);  // every MMA issued above completes before tensor memory is freed
+      drain_wait(&drain[0], 0);
+    } else if (warp == kPvWarp && lane == 0) {
+    // ------------------------------------------------------------ P~ V issuer (one lane)
+      constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
+      bool ok = true;
+      for (int j = 0; ok && j < T; ++j) {
+        // P~(j) V(j) once its P~ tile is written and the fold of tile j-2 has read R[j%2]
+        ok = mbar_wait<true>(&p_full[j & 1], (j >> 1) & 1, ab, kSitePFull) &&
+             (j < 2 || mbar_wait<true>(&r_free[j & 1], ((j - 2) >> 1) & 1, ab, kSiteRFree));
         if (!ok) break;
         tc_fence_after();
         const uint64_t vdesc = sdesc_kmajor(smem_u32(smem + P::kV + (j % ST) * DP * 128), 128);
-        const uint32_t aP = tbase + (sb ? kColP1 : kColP0);
+        const uint32_t d = tbase + ((j & 1) ? kColR1 : kColR0);
+        const uint32_t aP = tbase + ((j & 1) ? kColP1 : kColP0);  // P~(j) in tensor memory
 #pragma unroll
         for (int kk = 0; kk < kBKV / 32; ++kk)
-          mma_e4m3_ts(tbase + kColR, aP + kk * 8, vdesc + (uint64_t)(kk * 2), idesc_pv, kk > 0);
-        mma_commit(&pv_done[sb]);
+          mma_e4m3_ts(d, aP + kk * 8, vdesc + (uint64_t)(kk * 2), idesc_pv, kk > 0);
+        mma_commit(&pv_done[j & 1]);
+        // K(j) was read by QK(j), complete before the softmax of tile j began
         mma_commit(&kv_empty[j % ST]);
       }
-      mma_commit(drain);  // every MMA issued above completes before tensor memory is freed
-      drain_wait(drain, 0);
+      mma_commit(&drain[1]);
+      drain_wait(&drain[1], 0);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const int row = warp * 32 + lane;
+    cta_teardown(warp == kMmaWarp, tbase);
+  } else if (warp < kFoldWarp0) {
+    regs_acquire<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax (4 warps)
+    // thread t of softmax warp w owns accumulator row 32w+t (its TMEM lane), all 128 keys
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
     const int i = qt * kBQ + row;
     const bool row_ok = i < s.nq;
     const float c32 = g.c32;
@@ -270,24 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         row_ok ? __fmul_rn(a.qscale[(size_t)hq * a.L.Tq + s.qpad0 + qt * kBQ + row], c32) : 0.f;
     const int last_key = g.causal ? min(i + (s.nkv - s.nq), s.nkv - 1) : s.nkv - 1;
     const float L32 = 8.8073549220576041f;  // fl32(log2(448))
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    {  // this row's Q codes (Dp bytes) into tensor memory: the A operand of Q K^T
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t tS = tbase + lane_base + kColS;
+    {  // the row's Q codes into tensor memory: the A operand of Q K^T
       const uint4 *qrow = reinterpret_cast<const uint4 *>(
           a.qcode + ((size_t)hq * a.L.Tq + s.qpad0 + qt * kBQ + row) * DP);
-      uint32_t qw[DP / 4];
 #pragma unroll
-      for (int c = 0; c < DP / 16; ++c) {
-        const uint4 u = __ldg(qrow + c);
-        qw[4 * c] = u.x;
-        qw[4 * c + 1] = u.y;
-        qw[4 * c + 2] = u.z;
-        qw[4 * c + 3] = u.w;
-      }
-#pragma unroll
-      for (int c = 0; c < DP / 32; ++c) {
-        uint32_t w8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w8[e] = qw[8 * c + e];
+      for (int c = 0; c < DP / 32; ++c) {  // 32 bytes = 8 words per store
+        const uint4 u0 = __ldg(qrow + 2 * c), u1 = __ldg(qrow + 2 * c + 1);
+        const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
         tmem_st8(tbase + lane_base + kColQ + 8 * c, w8);
       }
       tmem_st_wait();
@@ -295,157 +340,171 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
-    // Every decision to continue is warp-uniform: after each wait the warp takes lane 0's result.
-    bool ok = true;
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; ok && j < T; ++j) {
-      const int sb = j & 1, st = j % ST;
-      // S(j) computed, its ring stage loaded, and P~[sb] no longer read by PV(j-2)
-      ok = mbar_wait(&s_full[sb], (j >> 1) & 1, ab, kSiteSFull) &&
-           mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm) &&
-           (j < 2 || mbar_wait(&pv_done[sb], ((j - 2) >> 1) & 1, ab, kSitePvDone));
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tS = tbase + lane_base + (sb ? kColS1 : kColS0);
-      const uint32_t tP = tbase + lane_base + (sb ? kColP1 : kColP0);
+    // Latency overlap without carrying S across tiles: the load of S(j) is issued first and this
+    // tile's other waits are tried while it is in flight; tile j-1's P~ (stored at its end) is
+    // handed over to the MMA after the load, by when the store has landed.
+    float alpha_prev = 1.f;
+    int jprev = -1;  // tile whose P~ store is still to be handed over
+    auto hand_over = [&]() {
+      tmem_st_wait();
+      tc_fence_before();
+      alpha_ring[(jprev & 3) * 128 + row] = alpha_prev;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&p_full[jprev & 1]);
+        mbar_arrive(&a_full[jprev & 3]);
+      }
+      jprev = -1;
+    };
+#pragma unroll 1
+    for (int j = 0; j < T; ++j) {
+      const int st = j % ST;
+      const int pb = j & 1;
+      bool ok = warp_all(mbar_wait(s_full, j & 1, ab, kSiteSFull));
       uint32_t v[128];
-      tmem_ld128(tS, v);
-      // S(j) is in registers: the MMA warp may compute S(j+2) into this buffer
+      if (ok) {
+        tc_fence_after();
+        tmem_ld128_nowait(tS, v);
+      }
+      if (!ok) {
+        if (jprev >= 0) hand_over();
+        break;
+      }
+      // this tile's K scales and DeltaS, and the P~ tile [j%2] free (PV(j-2) complete): one
+      // try each while the load is in flight, the bounded wait after it if needed (keep loops,
+      // barriers and tcgen05 waits out of the span between a load and its wait: ptxas then
+      // spills the 128 pending registers)
+      const bool kv_ready = mbar_try_wait(&kv_full[st], (j / ST) & 1);
+      const bool pv_ready = (j < 2) || mbar_try_wait(&pv_done[pb], ((j - 2) >> 1) & 1);
+      tmem_wait_ld128(v);  // S(j) is in registers
+      if (jprev >= 0) hand_over();  // tile j-1's P~ store has long landed by now
+      ok = warp_all((kv_ready || mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm)) &&
+                    (pv_ready || mbar_wait(&pv_done[pb], ((j - 2) >> 1) & 1, ab, kSitePvDone)));
+      if (!ok) break;
+      // QK(j+1) may overwrite S
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+      if (lane == 0) mbar_arrive(s_free);
       if (DBG && j == a.dbg.kt) {
 #pragma unroll
         for (int e = 0; e < 128; ++e) a.dbg.s_out[row * 128 + e] = __uint_as_float(v[e]);
       }
       const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 512);
       const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
-      const int lim = last_key - j * kBKV;  // columns 0..lim are visible to this row
-      // The arithmetic below runs in long independent phases over the 128 values, in place,
-      // so the scheduler can keep the FMA and MUFU pipes busy with one warp.
+      const int lim = last_key - j * kBKV;  // keys 0..lim of this tile are visible
       float x[128];
+      float pmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // S' = A * (s_q c s_k) + DeltaS c
-        const float mult = __fmul_rn(sqc, skv[c]);
+      for (int h = 0; h < 2; ++h) {
+        float xh[64];
+        uint32_t vh[64];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = *reinterpret_cast<const float4 *>(dsc + c * 32 + e);
-          const int k0 = c * 32 + e;
-          fma2(x[k0], x[k0 + 1], __uint_as_float(v[k0]), __uint_as_float(v[k0 + 1]), mult, mult,
-               d4.x, d4.y);
-          fma2(x[k0 + 2], x[k0 + 3], __uint_as_float(v[k0 + 2]), __uint_as_float(v[k0 + 3]), mult,
-               mult, d4.z, d4.w);
-        }
+        for (int e = 0; e < 64; ++e) vh[e] = v[64 * h + e];
+        pmax = fmaxf(pmax, logits64(xh, vh, dsc + 64 * h, skv + 2 * h, sqc, lim - 64 * h));
+#pragma unroll
+        for (int e = 0; e < 64; ++e) x[64 * h + e] = xh[e];
       }
-      if (lim < kBKV - 1) {  // diagonal / ragged tile: hide the keys this row does not see
-#pragma unroll
-        for (int e = 0; e < 128; ++e) x[e] = (e <= lim) ? x[e] : -INFINITY;
-      }
-      // row maximum: eight independent 3-input max chains, then a small tree
-      float mk[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[16 * k], x[16 * k + 1]);
-#pragma unroll
-      for (int e = 2; e < 16; e += 2)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mk[k] = max3(mk[k], x[16 * k + e], x[16 * k + e + 1]);
-      const float m_new = max3(max3(mk[0], mk[1], mk[2]), max3(mk[3], mk[4], mk[5]),
-                               max3(mk[6], mk[7], m));
-      const float m448 = (m_new == -INFINITY) ? 0.f : __fsub_rn(m_new, L32);
-      const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(__fsub_rn(m, m_new));
+      const float m_new = fmaxf(m, pmax);
+      const bool none = (m_new == -INFINITY);  // no visible key so far in this row
+      const float alpha = none ? 1.f : ex2_approx(__fsub_rn(m, m_new));
+      const float m448 = none ? 0.f : __fsub_rn(m_new, L32);
       // P448 = 2^(S' - m448); masked keys have S' = -inf and give 0
 #pragma unroll
       for (int e = 0; e < 128; e += 2) add2(x[e], x[e + 1], x[e], x[e + 1], -m448, -m448);
 #pragma unroll
       for (int e = 0; e < 128; ++e) x[e] = ex2_approx(x[e]);
-      float ps[8][2];  // row sum: eight independent packed accumulators
+      float ps[4][2];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ps[k][0] = ps[k][1] = 0.f;
+      for (int k = 0; k < 4; ++k) ps[k][0] = ps[k][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 128; e += 2)
-        add2(ps[(e >> 1) & 7][0], ps[(e >> 1) & 7][1], ps[(e >> 1) & 7][0], ps[(e >> 1) & 7][1],
+        add2(ps[(e >> 1) & 3][0], ps[(e >> 1) & 3][1], ps[(e >> 1) & 3][0], ps[(e >> 1) & 3][1],
              x[e], x[e + 1]);
-      uint32_t pk[32];  // P~ = e4m3(P448), four keys per word
+      const float rs = __fadd_rn(
+          __fadd_rn(__fadd_rn(ps[0][0], ps[0][1]), __fadd_rn(ps[1][0], ps[1][1])),
+          __fadd_rn(__fadd_rn(ps[2][0], ps[2][1]), __fadd_rn(ps[3][0], ps[3][1])));
+      // P~ = e4m3(P448): 128 keys -> 32 words, into the P~ tile [j%2] in tensor memory; it is
+      // handed over to the MMA at the top of the next tile (or after the last one)
+      uint32_t pk[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e)
         pk[e] = cvt_e4m3x2(x[4 * e], x[4 * e + 1]) | (cvt_e4m3x2(x[4 * e + 2], x[4 * e + 3]) << 16);
-      tmem_st32(tP, pk);
+      tmem_st32(tbase + lane_base + (pb ? kColP1 : kColP0), pk);
       if (DBG && j == a.dbg.kt) {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          *reinterpret_cast<uint32_t *>(a.dbg.p_out + row * 128 + e * 4) = pk[e];
+          *reinterpret_cast<uint32_t *>(a.dbg.p_out + row * 128 + 4 * e) = pk[e];
       }
-      tmem_st_wait();
-      tc_fence_before();
-      alpha_ring[(j & 3) * 128 + row] = alpha;
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&p_full[sb]);
-        mbar_arrive(&a_full[j & 3]);
-      }
-      float psum[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        psum[k] = __fadd_rn(__fadd_rn(ps[2 * k][0], ps[2 * k][1]), __fadd_rn(ps[2 * k + 1][0], ps[2 * k + 1][1]));
-      l = __fmaf_rn(alpha, l, __fadd_rn(__fadd_rn(psum[0], psum[1]), __fadd_rn(psum[2], psum[3])));
+      alpha_prev = alpha;
+      jprev = j;
+      l = __fmaf_rn(alpha, l, rs);
       m = m_new;
     }
+    if (jprev >= 0) hand_over();
     lsum[row] = l;
     __syncwarp();
     if (lane == 0) mbar_arrive(l_full);
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ fold + epilogue (warps 4-7)
-    const int q4 = warp - 4;
-    const int row = q4 * 32 + lane;
+    cta_teardown(false, tbase);
+  } else {
+    regs_acquire<kRegsFold>();
+    // ------------------------------------------------------------ fold + epilogue (4 warps)
+    // thread t of fold warp w folds row 32w+t: O = alpha O + R, O in registers
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
     const int i = qt * kBQ + row;
     const bool row_ok = i < s.nq;
-    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     float O[DP];
 #pragma unroll
     for (int d = 0; d < DP; ++d) O[d] = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(&a_full[j & 3], (j >> 2) & 1, ab, kSiteAFull);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ok = warp_all(mbar_wait<true>(&a_full[j & 3], (j >> 2) & 1, ab, kSiteAFull));
       if (!ok) break;
       const float alpha = alpha_ring[(j & 3) * 128 + row];
-      ok = mbar_wait(&pv_done[j & 1], (j >> 1) & 1, ab, kSiteRFull);  // R(j) is complete
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ok = warp_all(mbar_wait<true>(&pv_done[j & 1], (j >> 1) & 1, ab, kSiteRFull));  // R(j) complete
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tR = tbase + lane_base + kColR;
+      const uint32_t tR = tbase + lane_base + ((j & 1) ? kColR1 : kColR0);
 #pragma unroll
-      for (int c = 0; c < DP / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16_wait(tR + c * 16, v);
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32_wait(tR + 32 * c, r);
+        if (c == DP / 32 - 1) {  // R[j%2] is read: PV(j+2) may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&r_free[j & 1]);
+        }
         if (DBG && j == a.dbg.kt) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) a.dbg.r_out[row * DP + c * 16 + e] = __uint_as_float(v[e]);
+          for (int e = 0; e < 32; ++e) a.dbg.r_out[row * DP + 32 * c + e] = __uint_as_float(r[e]);
         }
 #pragma unroll
-        for (int e = 0; e < 16; e += 2)
-          fma2(O[c * 16 + e], O[c * 16 + e + 1], alpha, alpha, O[c * 16 + e], O[c * 16 + e + 1],
-               __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+        for (int e = 0; e < 32; e += 2)
+          fma2(O[32 * c + e], O[32 * c + e + 1], alpha, alpha, O[32 * c + e], O[32 * c + e + 1],
+               __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(r_free);
     }
     if (ok) ok = mbar_wait(l_full, 0, ab, kSiteLFull);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    ok = warp_all(ok);
     // ------------------------------------------------------------ epilogue
-    if (ok && row_ok && !*abort_flag) {
+    if (warp_all(ok && !*abort_flag)) {
       const float l = lsum[row];
       const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
       const float *svp = a.vscale + ((size_t)b * g.Hkv + hk) * DP;
       const size_t o = (out_row0 + (size_t)row * g.Hq) * g.D0;
 #pragma unroll
-      for (int d = 0; d < DP; d += 8) {
-        if (d < g.D0) {
+      for (int c = 0; c < DP / 8; ++c) {
+        const int d = 8 * c;
+        if (row_ok && d < g.D0) {
+          // the 8 channel scales, loaded right here (a volatile load is not hoisted next to
+          // the whole O row, which would not fit the fold warps' registers)
+          const float4 s0 = ldg_nc_v4(svp + d), s1 = ldg_nc_v4(svp + d + 4);
+          const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
           float y[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(O[d + e], svp[d + e]), inv_l);
+          for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(O[d + e], sv[e]), inv_l);
           if (a.out_dtype == SAGE2_FP32) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + o + d);
             dst[0] = make_float4(y[0], y[1], y[2], y[3]);
@@ -470,14 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    cta_teardown(false, tbase);
   }
-
-  // ------------------------------------------------------------ teardown
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tbase, kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
