@@ -49,7 +49,21 @@
 namespace sage2 {
 namespace {
 
-constexpr int kTmaWarp = 0, kMmaWarp = 1, kPvWarp = 2, kSmWarp0 = 4, kFoldWarp0 = 8;
+#ifndef SAGE2_TMA_WARP
+#define SAGE2_TMA_WARP 0
+#endif
+#ifndef SAGE2_QK_WARP
+#define SAGE2_QK_WARP 1
+#endif
+#ifndef SAGE2_PV_WARP
+#define SAGE2_PV_WARP 2
+#endif
+constexpr int kTmaWarp = SAGE2_TMA_WARP, kMmaWarp = SAGE2_QK_WARP, kPvWarp = SAGE2_PV_WARP,
+              kSmWarp0 = 4, kFoldWarp0 = 8;
+static_assert(kTmaWarp >= 0 && kTmaWarp < 4 && kMmaWarp >= 0 && kMmaWarp < 4 && kPvWarp >= 0 &&
+                  kPvWarp < 4 && kTmaWarp != kMmaWarp && kTmaWarp != kPvWarp &&
+                  kMmaWarp != kPvWarp,
+              "the producer and the issuers are distinct warps of the control warpgroup");
 constexpr int kNumWarps = 12, kThreads = 32 * kNumWarps;
 // Registers per thread after the split (the launch gives every warpgroup 128; setmaxnreg.inc
 // waits until the other warpgroups have released enough, so the sum must stay within 4 x 128).
