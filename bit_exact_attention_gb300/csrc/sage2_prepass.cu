@@ -256,12 +256,17 @@ __global__ void __launch_bounds__(256) v_quant(PrepassArgs a) {
 }
 
 // ------------------------------------------------------------------ 4. Q codes
-// grid (ceil(max_nq / 128), Hq, B), block 128: warp w owns rows 32w .. 32w + 31 of the
-// block, lane l channels [l * CPL, l * CPL + CPL).
+// grid (ceil(max_nq / 128), Hq, B), block 256. The block's 128 x D0 input values are staged in
+// shared memory with asynchronous 16-byte copies (few registers, so many CTAs per SM keep enough
+// loads in flight). Channel sums: thread t sums channel t % DP over one half of the rows in
+// double-float; the two halves are combined in double. The sums are exact for 16-bit inputs, so
+// the mean is the definition's fl32(sum / n). Quantization: warp w owns rows 16w .. 16w + 15,
+// lane l channels [l * CPL, l * CPL + CPL).
 template <int DP>
-__global__ void __launch_bounds__(128) q_quant(PrepassArgs a) {
-  constexpr int CPL = DP / 32;
-  __shared__ double colsum[4][DP];
+__global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
+  constexpr int CPL = DP / 32, RPW = 16;
+  __shared__ __align__(16) uint16_t blk[kBQ][DP];  // rows past the end / channels past D0: 0
+  __shared__ double colsum[2][DP];
   __shared__ float qbar[DP];
   const Geometry &g = a.g;
   const int b = blockIdx.z, h = blockIdx.y, qb = blockIdx.x;
@@ -271,69 +276,77 @@ __global__ void __launch_bounds__(128) q_quant(PrepassArgs a) {
     return;
   }
   if (qb * kBQ >= ((s.nq + kBQ - 1) / kBQ) * kBQ) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c0 = lane * CPL;
-  const bool chan_ok = c0 < g.D0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t row_elems = (size_t)g.Hq * g.D0;
-  float x[32][CPL];
-  float hi[CPL], lo[CPL];
-#pragma unroll
-  for (int e = 0; e < CPL; ++e) hi[e] = lo[e] = 0.f;
-#pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const int i = qb * kBQ + warp * 32 + r;
-    float val[CPL];
-#pragma unroll
-    for (int e = 0; e < CPL; ++e) val[e] = 0.f;
-    if (i < s.nq && chan_ok) {
-      const uint16_t *src = a.q + (size_t)(s.q0 + i) * row_elems + (size_t)h * g.D0 + c0;
-      if (CPL == 4) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(src));
-        val[0] = to_f32((uint16_t)(u.x & 0xFFFFu), a.bf16);
-        val[1] = to_f32((uint16_t)(u.x >> 16), a.bf16);
-        val[2] = to_f32((uint16_t)(u.y & 0xFFFFu), a.bf16);
-        val[3] = to_f32((uint16_t)(u.y >> 16), a.bf16);
-      } else {
-        const uint32_t u = __ldg(reinterpret_cast<const uint32_t *>(src));
-        val[0] = to_f32((uint16_t)(u & 0xFFFFu), a.bf16);
-        val[1] = to_f32((uint16_t)(u >> 16), a.bf16);
-      }
-#pragma unroll
-      for (int e = 0; e < CPL; ++e) df_add(hi[e], lo[e], val[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < CPL; ++e) x[r][e] = val[e];
-  }
-#pragma unroll
-  for (int e = 0; e < CPL; ++e) colsum[warp][c0 + e] = (double)hi[e] + (double)lo[e];
-  __syncthreads();
   const int nvalid = min(kBQ, s.nq - qb * kBQ);
-  for (int d = threadIdx.x; d < DP; d += blockDim.x) {
-    const double sum = ((colsum[0][d] + colsum[1][d]) + colsum[2][d]) + colsum[3][d];
+  // stage: 8-element (16-byte) chunks; D0 % 8 == 0, so a chunk is wholly inside or outside
+  constexpr int kChunks = DP / 8;
+  for (int c = tid; c < kBQ * kChunks; c += blockDim.x) {
+    const int r = c / kChunks, ch = (c % kChunks) * 8;
+    uint16_t *dst = &blk[r][ch];
+    if (r < nvalid && ch < g.D0) {
+      const uint16_t *src = a.q + (size_t)(s.q0 + qb * kBQ + r) * row_elems + (size_t)h * g.D0 + ch;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                   : "memory");
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  {  // channel sums: thread t, channel t % DP, rows [half * 64, half * 64 + 64) (256 / DP halves)
+    constexpr int kParts = 256 / DP, kRowsPer = kBQ / kParts;
+    const int d = tid % DP, part = tid / DP;
+    float hi = 0.f, lo = 0.f;
+#pragma unroll 8
+    for (int r = part * kRowsPer; r < (part + 1) * kRowsPer; ++r)
+      df_add(hi, lo, to_f32(blk[r][d], a.bf16));  // staged zeros add nothing
+    if (kParts == 2) {
+      colsum[part][d] = (double)hi + (double)lo;
+    } else {  // DP = 64: four parts, folded pairwise into the two slots
+      __shared__ double part4[4][64];
+      part4[part][d] = (double)hi + (double)lo;
+      __syncthreads();
+      if (part < 2) colsum[part][d] = part4[2 * part][d] + part4[2 * part + 1][d];
+    }
+  }
+  __syncthreads();
+  for (int d = tid; d < DP; d += blockDim.x) {
+    const double sum = colsum[0][d] + colsum[1][d];
     const float m = (nvalid > 0 && d < g.D0) ? (float)(sum / (double)nvalid) : 0.f;
     qbar[d] = m;
     a.w.qmean[((size_t)h * a.L.nqblk + s.qpad0 / kBQ + qb) * DP + d] = m;
   }
   __syncthreads();
+  // Q~ = fl32(Q - qbar); one scale per row (the row spans the warp's 32 lanes)
+  const int c0 = lane * CPL;
+  const bool chan_ok = c0 < g.D0;
   float mb[CPL];
 #pragma unroll
   for (int e = 0; e < CPL; ++e) mb[e] = qbar[c0 + e];
-  const size_t row0 = (size_t)h * a.L.Tq + s.qpad0 + qb * kBQ + warp * 32;
+  const int rbase = warp * RPW;  // row within the block
+  float amax[RPW];
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const int i = qb * kBQ + warp * 32 + r;
-    const bool rv = i < s.nq && chan_ok;
+  for (int r = 0; r < RPW; ++r) {
+    const bool rv = rbase + r < nvalid && chan_ok;
+    amax[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e)
+      amax[r] = fmaxf(amax[r], fabsf(rv ? __fsub_rn(to_f32(blk[rbase + r][c0 + e], a.bf16), mb[e]) : 0.f));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], off));
+  const size_t row0 = (size_t)h * a.L.Tq + s.qpad0 + qb * kBQ + rbase;
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const bool rv = rbase + r < nvalid && chan_ok;
     float xt[CPL];
-    float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) {
-      xt[e] = rv ? __fsub_rn(x[r][e], mb[e]) : 0.f;
-      amax = fmaxf(amax, fabsf(xt[e]));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float inv = amax > 0.f ? __fdiv_rn(7.f, amax) : 0.f;
+    for (int e = 0; e < CPL; ++e)
+      xt[e] = rv ? __fsub_rn(to_f32(blk[rbase + r][c0 + e], a.bf16), mb[e]) : 0.f;
+    const float inv = amax[r] > 0.f ? __fdiv_rn(7.f, amax[r]) : 0.f;
     uint8_t *dst = a.w.qcode + (row0 + r) * DP + c0;
     if (CPL == 4) {
       const uint32_t lo2 = cvt_e4m3x2(int4_code(xt[0], inv), int4_code(xt[1], inv));
@@ -343,7 +356,7 @@ __global__ void __launch_bounds__(128) q_quant(PrepassArgs a) {
       *reinterpret_cast<uint16_t *>(dst) =
           (uint16_t)cvt_e4m3x2(int4_code(xt[0], inv), int4_code(xt[1], inv));
     }
-    if (lane == 0) a.w.qscale[row0 + r] = amax > 0.f ? __fdiv_rn(amax, 7.f) : 0.f;
+    if (lane == 0) a.w.qscale[row0 + r] = amax[r] > 0.f ? __fdiv_rn(amax[r], 7.f) : 0.f;
   }
 }
 
@@ -500,12 +513,12 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   if (g.Dp == 128) {
     k_quant<128><<<kv_grid, 128, 0, st>>>(a);
     v_quant<128><<<kv_grid, 256, 0, st>>>(a);
-    q_quant<128><<<q_grid, 128, 0, st>>>(a);
+    q_quant<128><<<q_grid, 256, 0, st>>>(a);
     delta_s<128><<<ds_grid, 256, 0, st>>>(a);
   } else {
     k_quant<64><<<kv_grid, 128, 0, st>>>(a);
     v_quant<64><<<kv_grid, 256, 0, st>>>(a);
-    q_quant<64><<<q_grid, 128, 0, st>>>(a);
+    q_quant<64><<<q_grid, 256, 0, st>>>(a);
     delta_s<64><<<ds_grid, 256, 0, st>>>(a);
   }
   return cudaGetLastError();
