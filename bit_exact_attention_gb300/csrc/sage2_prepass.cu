@@ -457,7 +457,8 @@ __global__ void __launch_bounds__(256) delta_s(PrepassArgs a) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(qq[i], kk[j], acc[i][j]);
+        for (int j = 0; j < 8; j += 2)  // packed: two independent, correctly rounded FMAs
+          fma2(acc[i][j], acc[i][j + 1], qq[i], qq[i], kk[j], kk[j + 1], acc[i][j], acc[i][j + 1]);
     }
   }
 
