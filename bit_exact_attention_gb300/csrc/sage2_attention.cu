@@ -391,15 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // spills the 128 pending registers)
       const bool kv_ready = mbar_try_wait(&kv_full[st], (j / ST) & 1);
       const bool pv_ready = (j < 2) || mbar_try_wait(&pv_done[pb], ((j - 2) >> 1) & 1);
-      tmem_wait_ld128(v);  // S(j) is in registers
+      tmem_wait_ld128(v);  // S(j) is in registers: QK(j+1) may overwrite S
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
       if (jprev >= 0) hand_over();  // tile j-1's P~ store has long landed by now
       ok = warp_all((kv_ready || mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm)) &&
                     (pv_ready || mbar_wait(&pv_done[pb], ((j - 2) >> 1) & 1, ab, kSitePvDone)));
       if (!ok) break;
-      // QK(j+1) may overwrite S
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
       if (DBG && j == a.dbg.kt) {
 #pragma unroll
         for (int e = 0; e < 128; ++e) a.dbg.s_out[row * 128 + e] = __uint_as_float(v[e]);
