@@ -60,6 +60,7 @@ namespace {
 #endif
 constexpr int kTmaWarp = SAGE2_TMA_WARP, kMmaWarp = SAGE2_QK_WARP, kPvWarp = SAGE2_PV_WARP,
               kSmWarp0 = 4, kFoldWarp0 = 8;
+static_assert(kSmWarp0 == 4 && kFoldWarp0 == 8, "softmax warps 4-7, fold warps 8-11");
 static_assert(kTmaWarp >= 0 && kTmaWarp < 4 && kMmaWarp >= 0 && kMmaWarp < 4 && kPvWarp >= 0 &&
                   kPvWarp < 4 && kTmaWarp != kMmaWarp && kTmaWarp != kPvWarp &&
                   kMmaWarp != kPvWarp,
@@ -105,7 +106,8 @@ struct SmemPlan {
   static constexpr int kSk = kDsc + ST * 512;            // float [ST][4]
   static constexpr int kAlpha = kSk + ST * 16;           // float [4][128]
   static constexpr int kLsum = kAlpha + 4 * 128 * 4;     // float [128]
-  static constexpr int kBar = kLsum + 128 * 4;
+  static constexpr int kSv = kLsum + 128 * 4;            // float [4 fold warps][DP]
+  static constexpr int kBar = kSv + 4 * DP * 4;
   // q, full[ST], empty[ST], s_full, s_free, p_full[2], pv_done[2], r_free[2], a[4], l, drain[2]
   static constexpr int kNumBars = 1 + 2 * ST + 1 + 1 + 2 + 2 + 2 + 4 + 1 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
@@ -468,6 +470,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = qt * kBQ + row;
     const bool row_ok = i < s.nq;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    // the V channel scales into this warp's own slice of shared memory now, so that the
+    // epilogue does not wait on global loads
+    float *sv_s = reinterpret_cast<float *>(smem + P::kSv) + qd * DP;
+    {
+      const float *svp = a.vscale + ((size_t)b * g.Hkv + hk) * DP;
+      for (int c = lane; c < DP; c += 32) sv_s[c] = __ldg(svp + c);
+    }
     float O[DP];
 #pragma unroll
     for (int d = 0; d < DP; ++d) O[d] = 0.f;
@@ -505,15 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp_all(ok && !*abort_flag)) {
       const float l = lsum[row];
       const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
-      const float *svp = a.vscale + ((size_t)b * g.Hkv + hk) * DP;
       const size_t o = (out_row0 + (size_t)row * g.Hq) * g.D0;
+      __syncwarp();  // the slice of channel scales is complete
 #pragma unroll
       for (int c = 0; c < DP / 8; ++c) {
         const int d = 8 * c;
         if (row_ok && d < g.D0) {
-          // the 8 channel scales, loaded right here (a volatile load is not hoisted next to
-          // the whole O row, which would not fit the fold warps' registers)
-          const float4 s0 = ldg_nc_v4(svp + d), s1 = ldg_nc_v4(svp + d + 4);
+          const float4 s0 = *reinterpret_cast<const float4 *>(sv_s + d);
+          const float4 s1 = *reinterpret_cast<const float4 *>(sv_s + d + 4);
           const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
           float y[8];
 #pragma unroll
