@@ -66,12 +66,12 @@ def _load():
         lib.oracle_num_threads.restype = i
         lib.oracle_attention_exact.argtypes = [P, P, P, i, i, P, P, i, i, i, i, f, i, P, i, P]
         lib.oracle_kv_stats.argtypes = [P, P, i, i, P, i, i, i, P, P]
-        lib.oracle_quant_q.argtypes = [P, i, i, P, i, i, i, i, i, P, P, P]
+        lib.oracle_quant_q.argtypes = [P, i, i, P, i, i, i, i, i, i, P, P, P]
         lib.oracle_quant_k.argtypes = [P, i, i, P, i, i, i, i, P, P, P]
         lib.oracle_quant_v.argtypes = [P, i, i, P, i, i, i, P, P, P]
         lib.oracle_delta_s.argtypes = [P, i, P, i, i, i, i, i, P, P, P]
         lib.oracle_attention_emulated.argtypes = [P, P, P, i, i, P, P, i, i, i, i, i, f, i, i, i,
-                                                  i, i, i, P, i, P]
+                                                  i, i, i, i, P, i, P, i, P]
         _lib = lib
         return lib
 
@@ -167,7 +167,7 @@ def kv_stats(k, v, dtype, cu_kv, Hkv, D0):
     return kmean, vamax
 
 
-def quant_q(q, dtype, cu_q, Hq, D0, bq=128, smooth_q=True):
+def quant_q(q, dtype, cu_q, Hq, D0, bq=128, smooth_q=True, per_block=False):
     q = _u16(q)
     cq = _cu(cu_q)
     B, Dp = len(cq) - 1, padded_dim(D0)
@@ -176,7 +176,7 @@ def quant_q(q, dtype, cu_q, Hq, D0, bq=128, smooth_q=True):
     codes = np.zeros((int(cq[-1]), Hq, Dp), np.int8)
     sq = np.zeros((int(cq[-1]), Hq), np.float32)
     _load().oracle_quant_q(_ptr(q), dtype, B, _ptr(cq), Hq, D0, Dp, bq, int(bool(smooth_q)),
-                           _ptr(qmean), _ptr(codes), _ptr(sq))
+                           int(bool(per_block)), _ptr(qmean), _ptr(codes), _ptr(sq))
     return qmean, codes, sq
 
 
@@ -219,8 +219,13 @@ def delta_s(k, dtype, cu_kv, b, Hkv, hk, D0, kmean, qbar):
 # ---------------------------------------------------------------- Mode Q
 def attention_emulated(q, k, v, dtype, cu_q, cu_kv, Hq, Hkv, D0, causal, sm_scale=0.0,
                        units=None, bq=128, bkv=128, gk=32, smooth_q=True, smooth_k=True,
-                       acc_bits=0, out=None) -> np.ndarray:
-    """The full quantized pipeline (FP64 result before output rounding)."""
+                       per_block=False, acc_bits=0, out=None) -> np.ndarray:
+    """The full quantized pipeline (FP64 result before output rounding).
+
+    Ablations (the defaults are the method): ``smooth_q`` / ``smooth_k`` off skip the Q block
+    mean / K channel mean; ``per_block`` gives Q one scale per block of ``bq`` rows and K one
+    per block of ``bkv`` keys instead of the per-thread scales; ``acc_bits > 0`` swaps the
+    two-level P~V fold for one-level accumulation in an ``acc_bits``-bit significand."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     cq, ck = _cu(cu_q), _cu(cu_kv)
     B = len(cq) - 1
@@ -229,6 +234,27 @@ def attention_emulated(q, k, v, dtype, cu_q, cu_kv, Hq, Hkv, D0, causal, sm_scal
     u, nu = _units(units)
     _load().oracle_attention_emulated(
         _ptr(q), _ptr(k), _ptr(v), dtype, B, _ptr(cq), _ptr(ck), Hq, Hkv, D0, padded_dim(D0),
-        int(bool(causal)), float(sm_scale), bq, bkv, gk, int(bool(smooth_q)), int(bool(smooth_k)),
-        int(acc_bits), _ptr(u), nu, _ptr(out))
+        int(bool(causal)), float(sm_scale), bq, bkv, bkv if per_block else gk,
+        int(bool(smooth_q)), int(bool(smooth_k)), int(bool(per_block)), int(acc_bits), _ptr(u), nu,
+        _ptr(out), 0, None)
     return out
+
+
+def emulated_tile_p448(q, k, v, dtype, cu_q, cu_kv, Hq, Hkv, D0, causal, b, h, qb, kt,
+                       sm_scale=0.0, bq=128, bkv=128, gk=32, smooth_q=True, smooth_k=True,
+                       per_block=False) -> np.ndarray:
+    """The fl32 P448 = 448 * 2^(S' - m_new) of KV tile kt of unit (b, h, qb), as the Mode-Q
+    emulation computes it on the way to its output: [bq][bkv], 0 where a key is not visible
+    (rows past the sequence end stay 0). The e4m3 code of P~ is oracle.e4m3_encode of it."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    cq, ck = _cu(cu_q), _cu(cu_kv)
+    B = len(cq) - 1
+    out = np.zeros((int(cq[-1]), Hq, D0), dtype=np.float64)
+    dump = np.zeros((bq, bkv), np.float32)
+    u, nu = _units([(b, h, qb)])
+    _load().oracle_attention_emulated(
+        _ptr(q), _ptr(k), _ptr(v), dtype, B, _ptr(cq), _ptr(ck), Hq, Hkv, D0, padded_dim(D0),
+        int(bool(causal)), float(sm_scale), bq, bkv, bkv if per_block else gk,
+        int(bool(smooth_q)), int(bool(smooth_k)), int(bool(per_block)), 0, _ptr(u), nu,
+        _ptr(out), int(kt), _ptr(dump))
+    return dump

@@ -344,9 +344,13 @@ static void quant_group(const float *x, const size_t *idx, int n, int8_t *codes,
  * channels -- one accumulator row per thread in the tensor-memory layout,
  * the analogue of the per-thread scale ([P2] Per-Thread INT4 Geometry) [R].
  * smooth_q = 0 skips the smoothing (qmean = 0; ablation only).
+ * q_per_block = 1 replaces the per-row scale by one scale over all valid rows
+ * and channels of the block (the coarser per-block granularity that the
+ * per-thread scheme improves on, [P3] component 2; ablation only).
  * qmean [B][Hq][nqb_max][Dp], qcodes [total_q][Hq][Dp], sq [total_q][Hq]. */
 void oracle_quant_q(const uint16_t *q, int dtype, int B, const int *cu_q, int Hq, int D0, int Dp,
-                    int bq, int smooth_q, float *qmean, int8_t *qcodes, float *sq) {
+                    int bq, int smooth_q, int q_per_block, float *qmean, int8_t *qcodes,
+                    float *sq) {
   int max_nq = 0;
   for (int b = 0; b < B; b++)
     if (cu_q[b + 1] - cu_q[b] > max_nq) max_nq = cu_q[b + 1] - cu_q[b];
@@ -358,21 +362,46 @@ void oracle_quant_q(const uint16_t *q, int dtype, int B, const int *cu_q, int Hq
         const int nq = cu_q[b + 1] - cu_q[b];
         float *mean = qmean + (((size_t)b * Hq + h) * nqb + qb) * Dp;
         const int r0 = qb * bq, r1 = (qb + 1) * bq < nq ? (qb + 1) * bq : nq;
-        float xt[128];
-        size_t idx[128];
-        for (int d = 0; d < Dp; d++) idx[d] = (size_t)d;
+        if (r1 <= r0) {
+          for (int d = 0; d < Dp; d++) mean[d] = 0.f;
+          continue;
+        }
+        const int nr = r1 - r0;
+        /* the smoothed block, rows in order; idx addresses it row-major */
+        float *xt = (float *)malloc(sizeof(float) * (size_t)nr * Dp);
+        size_t *idx = (size_t *)malloc(sizeof(size_t) * (size_t)nr * Dp);
+        int8_t *ct = (int8_t *)malloc((size_t)nr * Dp);
         for (int d = 0; d < Dp; d++) {
           double sum = 0.0;
           if (d < D0)
             for (int r = r0; r < r1; r++) sum += in_val(q, tix(cu_q[b] + r, h, Hq, D0) + d, dtype);
-          mean[d] = (smooth_q && r1 > r0 && d < D0) ? (float)(sum / (double)(r1 - r0)) : 0.f;
+          mean[d] = (smooth_q && d < D0) ? (float)(sum / (double)nr) : 0.f;
         }
-        for (int r = r0; r < r1; r++) {
-          const size_t row = (size_t)(cu_q[b] + r) * Hq + h;
-          for (int d = 0; d < Dp; d++)
-            xt[d] = d < D0 ? (float)in_val(q, row * D0 + d, dtype) - mean[d] : 0.f;
-          quant_group(xt, idx, Dp, qcodes + row * Dp, sq + row);
+        for (int r = 0; r < nr; r++) {
+          const size_t row = (size_t)(cu_q[b] + r0 + r) * Hq + h;
+          for (int d = 0; d < Dp; d++) {
+            xt[(size_t)r * Dp + d] = d < D0 ? (float)in_val(q, row * D0 + d, dtype) - mean[d] : 0.f;
+            idx[(size_t)r * Dp + d] = (size_t)r * Dp + d;
+          }
         }
+        if (q_per_block) {
+          float sc;
+          quant_group(xt, idx, nr * Dp, ct, &sc);
+          for (int r = 0; r < nr; r++) {
+            const size_t row = (size_t)(cu_q[b] + r0 + r) * Hq + h;
+            memcpy(qcodes + row * Dp, ct + (size_t)r * Dp, Dp);
+            sq[row] = sc;
+          }
+        } else {
+          for (int r = 0; r < nr; r++) {
+            const size_t row = (size_t)(cu_q[b] + r0 + r) * Hq + h;
+            quant_group(xt, idx + (size_t)r * Dp, Dp, ct, sq + row);
+            memcpy(qcodes + row * Dp, ct + (size_t)r * Dp, Dp);
+          }
+        }
+        free(xt);
+        free(idx);
+        free(ct);
       }
 }
 
@@ -489,11 +518,16 @@ void oracle_delta_s(const uint16_t *k, int dtype, const int *cu_kv, int b, int H
  *               partial of the two-level scheme; the FP64 sum is exact)
  *     O[i,d]  = fl32(alpha O[i,d] + R[i,d])         (FP32 fold)
  *   out[i,d] = O[i,d] * sv[d] / l   (FP64; 0 when no key is visible).
- * Flags (ablations; 1,1,0 is the method): smooth_q, smooth_k; acc_bits > 0
+ * Flags (ablations; smooth_q = smooth_k = 1, q_per_block = acc_bits = 0 is
+ * the method): smooth_q, smooth_k; q_per_block (one Q scale per block, see
+ * oracle_quant_q; with gk = bkv K gets one scale per block too); acc_bits > 0
  * replaces the two-level fold by one-level accumulation whose accumulator is
  * rounded to acc_bits significand bits after every 32-key MMA step (an
  * emulation of a reduced-precision FP8 MMA accumulator).
- * out [total_q][Hq][D0] (FP64, rows outside `units` untouched). */
+ * out [total_q][Hq][D0] (FP64, rows outside `units` untouched).
+ * dump_p448 (may be NULL; then `units` names exactly one unit): receives the
+ * fl32 P448 of every (row, key) of KV tile dump_kt of that unit, [bq][bkv]
+ * row-major; keys that are not visible are left untouched (test hook). */
 static double round_bits(double x, int bits) {
   if (x == 0.0 || bits <= 0) return x;
   int e2;
@@ -505,8 +539,9 @@ static double round_bits(double x, int bits) {
 void oracle_attention_emulated(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
                                int B, const int *cu_q, const int *cu_kv, int Hq, int Hkv, int D0,
                                int Dp, int causal, float sm_scale, int bq, int bkv, int gk,
-                               int smooth_q, int smooth_k, int acc_bits, const int *units,
-                               int n_units, double *out) {
+                               int smooth_q, int smooth_k, int q_per_block, int acc_bits,
+                               const int *units, int n_units, double *out, int dump_kt,
+                               float *dump_p448) {
   const int g = Hq / Hkv;
   const float scale32 = sm_scale > 0.f ? sm_scale : (float)(1.0 / sqrt((double)D0));
   const float c32 = (float)(1.4426950408889634074 * (double)scale32);
@@ -530,7 +565,7 @@ void oracle_attention_emulated(const uint16_t *q, const uint16_t *k, const uint1
   double e4m3_val[256]; /* value of every e4m3 byte, from the decoder above */
   for (int c = 0; c < 256; c++) e4m3_val[c] = oracle_e4m3_decode((uint8_t)c);
   oracle_kv_stats(k, v, dtype, B, cu_kv, Hkv, D0, Dp, kmean, vamax);
-  oracle_quant_q(q, dtype, B, cu_q, Hq, D0, Dp, bq, smooth_q, qmean, qc, sq);
+  oracle_quant_q(q, dtype, B, cu_q, Hq, D0, Dp, bq, smooth_q, q_per_block, qmean, qc, sq);
   oracle_quant_k(k, dtype, B, cu_kv, Hkv, D0, Dp, gk, smooth_k ? kmean : NULL, kc, sk);
   oracle_quant_v(v, dtype, B, cu_kv, Hkv, D0, Dp, vamax, vc, sv);
 
@@ -600,6 +635,7 @@ void oracle_attention_emulated(const uint16_t *q, const uint16_t *k, const uint1
           if (sp[jj] != -INFINITY) {
             const float arg = sp[jj] - m448;
             const float p448 = (float)exp2((double)arg);
+            if (dump_p448 && t0 / bkv == dump_kt) dump_p448[(size_t)(i - r0) * bkv + jj] = p448;
             lsum += (double)p448;
             const double pt = round_to_format((double)p448, 4, -6, 448.0, 1); /* e4m3 value */
             const uint8_t *vj = vc + ((size_t)(cu_kv[b] + t0 + jj) * Hkv + hk) * Dp;

@@ -61,9 +61,12 @@ def quantize_group(x: np.ndarray):
     return codes, F32(a / F32(7.0))
 
 
-def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=128, gk=32):
+def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=128, gk=32,
+           smooth_q=True, smooth_k=True, per_block=False):
     """q, k, v: float64 arrays [tokens, heads, d0] holding the exact fp16/bf16 values.
-    Returns the FP64 output before dtype rounding, [total_q, hq, d0]."""
+    Returns the FP64 output before dtype rounding, [total_q, hq, d0].
+    Switches: smooth_q / smooth_k off use a zero mean; per_block quantizes each block of bq
+    query rows, and each block of bkv keys, with one scale."""
     g = hq // hkv
     scale32 = F32(sm_scale) if sm_scale > 0 else F32(1.0 / math.sqrt(d0))
     c32 = F32(1.4426950408889634 * float(scale32))
@@ -77,14 +80,15 @@ def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=
             K = k[cu_kv[b]:cu_kv[b + 1], hk, :]
             V = v[cu_kv[b]:cu_kv[b + 1], hk, :]
             kmean = np.array([F32(K[:, c].sum() / nkv) for c in range(d0)], dtype=F32) \
-                if nkv else np.zeros(d0, F32)
+                if (nkv and smooth_k) else np.zeros(d0, F32)
             Kt = (K.astype(F32) - kmean).astype(F32)              # smoothed K, float32
             kcodes = np.zeros((nkv, d0), np.int64)
             ksc = np.zeros(nkv, F32)
-            for t0 in range(0, nkv, gk):
-                cds, s = quantize_group(Kt[t0:t0 + gk])
-                kcodes[t0:t0 + gk] = cds
-                ksc[t0:t0 + gk] = s
+            kg = bkv if per_block else gk
+            for t0 in range(0, nkv, kg):
+                cds, s = quantize_group(Kt[t0:t0 + kg])
+                kcodes[t0:t0 + kg] = cds
+                ksc[t0:t0 + kg] = s
             vamax = np.abs(V).max(axis=0).astype(F32) if nkv else np.zeros(d0, F32)
             vinv = np.array([F32(448.0) / a if a > 0 else F32(0) for a in vamax], dtype=F32)
             vsc = np.array([a / F32(448.0) if a > 0 else F32(0) for a in vamax], dtype=F32)
@@ -93,7 +97,10 @@ def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=
             Q = q[cu_q[b]:cu_q[b + 1], h, :]
             for r0 in range(0, nq, bq):
                 rows = range(r0, min(r0 + bq, nq))
-                qbar = np.array([F32(Q[r0:r0 + bq, c].sum() / len(rows)) for c in range(d0)], F32)
+                qbar = np.array([F32(Q[r0:r0 + bq, c].sum() / len(rows)) for c in range(d0)], F32) \
+                    if smooth_q else np.zeros(d0, F32)
+                if per_block:
+                    blk_codes, blk_scale = quantize_group((Q[r0:r0 + bq].astype(F32) - qbar).astype(F32))
                 dS = []
                 for j in range(nkv):
                     acc = F32(0)
@@ -102,7 +109,7 @@ def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=
                     dS.append(acc)
                 for i in rows:
                     qt = (Q[i].astype(F32) - qbar).astype(F32)
-                    qc, qs = quantize_group(qt)
+                    qc, qs = (blk_codes[i - r0], blk_scale) if per_block else quantize_group(qt)
                     sqc = F32(qs * c32)
                     m = -math.inf
                     lsum = 0.0

@@ -383,21 +383,63 @@ def test_zero_rounding_error_reduces_to_exact(oracle_mod, with_means, causal):
         assert not np.allclose(bad, ex, rtol=1e-3)
 
 
+ABLATION_FLAGS = [dict(), dict(smooth_q=False), dict(smooth_k=False), dict(per_block=True),
+                  dict(smooth_q=False, smooth_k=False, per_block=True)]
+
+
+@pytest.mark.parametrize("flags", ABLATION_FLAGS, ids=["method", "noQs", "noKs", "block", "naive"])
 @pytest.mark.parametrize("case", [
     dict(nq=(5,), nkv=(7,), hq=2, hkv=1, d0=4, causal=False, dtype="fp16", dist="tiny"),
     dict(nq=(6, 3), nkv=(4, 8), hq=2, hkv=2, d0=8, causal=True, dtype="bf16", dist="outlier"),
     dict(nq=(8,), nkv=(5,), hq=1, hkv=1, d0=8, causal=True, dtype="bf16", dist="dit"),
 ])
-def test_brute_force_tiny_vs_restatement(oracle_mod, case):
+def test_brute_force_tiny_vs_restatement(oracle_mod, case, flags):
     w = W.Workload("bf", case["nq"], case["nkv"], case["hq"], case["hkv"], case["d0"],
                    case["dtype"], case["causal"], case["dist"], 21, varlen=True)
     x = W.make_inputs(w)
     dt = W.dtype_code(w)
     got = oracle_mod.attention_emulated(bits(x["q"]), bits(x["k"]), bits(x["v"]), dt, x["cu_q"],
-                                        x["cu_kv"], w.hq, w.hkv, w.d, w.causal, bq=4, bkv=4, gk=2)
+                                        x["cu_kv"], w.hq, w.hkv, w.d, w.causal, bq=4, bkv=4, gk=2,
+                                        **flags)
     ref = NR.mode_q(x["q"].double().numpy(), x["k"].double().numpy(), x["v"].double().numpy(),
-                    x["cu_q"], x["cu_kv"], w.hq, w.hkv, w.d, w.causal, bq=4, bkv=4, gk=2)
+                    x["cu_q"], x["cu_kv"], w.hq, w.hkv, w.d, w.causal, bq=4, bkv=4, gk=2, **flags)
     np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-9)
+
+
+def test_quant_q_per_block_invariants(oracle_mod):
+    """Per-block Q granularity: every valid row of a block carries the block's one scale,
+    which is the largest of the block's per-row scales (so some row reaches code +-7 and no
+    row's scale exceeds it); rounding stays within half a step; padding channels stay 0."""
+    w = W.scaled(W.PREFILL, (300,), (300,), hq=2, hkv=2)
+    x = W.make_inputs(w)
+    qm, qc_row, sq_row = oracle_mod.quant_q(bits(x["q"]), BF16, x["cu_q"], 2, 128)
+    qm_b, qc_blk, sq_blk = oracle_mod.quant_q(bits(x["q"]), BF16, x["cu_q"], 2, 128,
+                                              per_block=True)
+    np.testing.assert_array_equal(qm, qm_b)            # the smoothing does not depend on it
+    q64 = x["q"].double().numpy()
+    for h in range(2):
+        for qb in range(3):
+            rows = slice(qb * 128, min(300, qb * 128 + 128))
+            s_blk = sq_blk[rows, h]
+            assert len(set(s_blk.tolist())) == 1
+            assert s_blk[0] == sq_row[rows, h].max()
+            xt = (q64[rows, h].astype(np.float32) - qm[0, h, qb]).astype(np.float32)
+            _check_codes(xt, qc_blk[rows, h], s_blk[0])
+            # a row holding the block maximum gets the same codes either way
+            r_top = int(np.argmax(sq_row[rows, h]))
+            np.testing.assert_array_equal(qc_blk[rows, h][r_top], qc_row[rows, h][r_top])
+
+
+def test_per_block_of_one_row_is_per_row(oracle_mod):
+    """With one query row per block and one KV tile per K group, per-block granularity is
+    the per-row / per-group granularity: both runs must agree bit for bit."""
+    w = W.scaled(W.PREFILL, (40,), (70,), hq=2, hkv=1)
+    x = W.make_inputs(w)
+    a = _emu(oracle_mod, w, x, bq=1, bkv=32, gk=32, smooth_q=False)
+    b = _emu(oracle_mod, w, x, bq=1, bkv=32, smooth_q=False, per_block=True)
+    np.testing.assert_array_equal(a, b)
+    c = _emu(oracle_mod, w, x, bkv=32, per_block=True)   # 128-row Q blocks: differs
+    assert not np.array_equal(a, c)
 
 
 @pytest.mark.parametrize("nkv", [100, 200])
@@ -411,6 +453,27 @@ def test_tiling_one_and_two_kv_tiles_vs_restatement(oracle_mod, nkv):
     ref = NR.mode_q(x["q"].double().numpy(), x["k"].double().numpy(), x["v"].double().numpy(),
                     x["cu_q"], x["cu_kv"], 1, 1, 64, False)
     np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-9)
+
+
+def test_tile_p448_dump_rebuilds_the_output(oracle_mod):
+    """The P448 test hook: with one KV tile (Nkv <= 128) a row's output is the e4m3 codes of
+    its dumped P448 times the V codes, times the V scales, over the sum of the unquantized
+    P448; the row maximum is 448 (x = log2 448 at the maximal key); invisible keys stay 0."""
+    w = W.Workload("dump", (90,), (100,), 2, 1, 64, "fp16", True, "tiny", 5, varlen=True)
+    x = W.make_inputs(w)
+    args = (bits(x["q"]), bits(x["k"]), bits(x["v"]), F16, x["cu_q"], x["cu_kv"], 2, 1, 64, True)
+    out = oracle_mod.attention_emulated(*args)
+    p = oracle_mod.emulated_tile_p448(*args, b=0, h=1, qb=0, kt=0).astype(np.float64)
+    _, vamax = oracle_mod.kv_stats(bits(x["k"]), bits(x["v"]), F16, x["cu_kv"], 1, 64)
+    vc, sv = oracle_mod.quant_v(bits(x["v"]), F16, x["cu_kv"], 1, 64, vamax)
+    vval = oracle_mod.e4m3_decode(vc)[:, 0]                        # [100][64]
+    pt = oracle_mod.e4m3_decode(oracle_mod.e4m3_encode(p[:90, :100]))
+    for i in range(90):
+        vis = i + 10                                               # bottom-right causal
+        assert np.all(p[i, vis + 1:] == 0) and np.all(p[i, :vis + 1] > 0)
+        assert abs(p[i].max() - 448.0) <= 448.0 * 2.0 ** -20
+        want = (pt[i] @ vval) * sv[0, 0] / p[i].sum()
+        np.testing.assert_allclose(out[i, 1], want, rtol=1e-6, atol=1e-9)
 
 
 # ----------------------------------------------------------------- accuracy (ablations)
@@ -438,6 +501,19 @@ def test_smoothing_ablations_are_directional(oracle_mod, outlier_case):
     e_none = relL1(_emu(oracle_mod, w, x, smooth_q=False, smooth_k=False), ex)
     assert e_full < 0.2
     assert e_noq > 1.5 * e_full and e_nok > 1.5 * e_full and e_none > e_noq
+
+
+def test_per_thread_granularity_beats_per_block(oracle_mod, outlier_case):
+    """Per-thread INT4 scales err less than one scale per block, with or without smoothing;
+    the naive scheme (per-block, no smoothing) errs most (the pages' granularity claim)."""
+    w, x = outlier_case
+    ex = oracle_mod.attention_exact(bits(x["q"]), bits(x["k"]), bits(x["v"]), W.dtype_code(w),
+                                    x["cu_q"], x["cu_kv"], w.hq, w.hkv, w.d, w.causal)
+    e_thread = relL1(_emu(oracle_mod, w, x), ex)
+    e_block = relL1(_emu(oracle_mod, w, x, per_block=True), ex)
+    e_naive = relL1(_emu(oracle_mod, w, x, per_block=True, smooth_q=False, smooth_k=False), ex)
+    assert e_block > 1.2 * e_thread
+    assert e_naive > e_block
 
 
 def test_two_level_accumulation_beats_one_level(oracle_mod, outlier_case):
