@@ -22,10 +22,19 @@ from ._lib import BF16, FP16, FP32, Sage2Error, WsLayout  # noqa: F401
 __all__ = ["attn_fwd", "attn_fwd_varlen", "prepass", "attention", "prepass_varlen",
            "attention_varlen", "workspace_size", "workspace_layout", "device_status",
            "alloc_workspace", "debug_tile", "debug_timeout", "Sage2Error", "load_library",
-           "attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES"]
+           "attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "quant_flags", "QUANT_NO_SMOOTH_Q",
+           "QUANT_NO_SMOOTH_K", "QUANT_PER_BLOCK"]
 
 _DT = {torch.float16: FP16, torch.bfloat16: BF16, torch.float32: FP32}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # SAGE2_NOALLOC_SCRATCH_BYTES in include/sage2_attn.h
+# sage2_quant_flags in include/sage2_attn.h: accuracy ablations; 0 is the method
+QUANT_NO_SMOOTH_Q, QUANT_NO_SMOOTH_K, QUANT_PER_BLOCK = 1, 2, 4
+
+
+def quant_flags(smooth_q: bool = True, smooth_k: bool = True, per_block: bool = False) -> int:
+    """The sage2_quant_flags word for one ablation setting (all defaults: the method)."""
+    return ((0 if smooth_q else QUANT_NO_SMOOTH_Q) | (0 if smooth_k else QUANT_NO_SMOOTH_K)
+            | (QUANT_PER_BLOCK if per_block else 0))
 
 
 def load_library():
@@ -98,8 +107,23 @@ def _out(out, shape, dtype, device):
 
 
 def attn_fwd(q, k, v, causal=False, sm_scale=0.0, out=None, out_dtype=None, workspace=None,
-             stream=None):
-    """softmax(Q K^T * sm_scale) V the SageAttention2 way; q [B, Nq, Hq, D], k/v [B, Nkv, Hkv, D]."""
+             stream=None, quant_flags=0):
+    """softmax(Q K^T * sm_scale) V the SageAttention2 way; q [B, Nq, Hq, D], k/v [B, Nkv, Hkv, D].
+
+    ``quant_flags`` (see :func:`quant_flags`) selects an accuracy ablation; it runs the packed
+    prepass with those switches, then the same attention kernel."""
+    if quant_flags:
+        B, Nq, Hq, D = q.shape
+        _, Nkv, Hkv, _ = k.shape
+        dev = q.device
+        cu_q = torch.arange(0, (B + 1) * Nq, Nq, dtype=torch.int32, device=dev)
+        cu_kv = torch.arange(0, (B + 1) * Nkv, Nkv, dtype=torch.int32, device=dev)
+        o = attn_fwd_varlen(q.reshape(B * Nq, Hq, D), k.reshape(B * Nkv, Hkv, D),
+                            v.reshape(B * Nkv, Hkv, D), cu_q, cu_kv, Nq, Nkv, causal=causal,
+                            sm_scale=sm_scale, out=None if out is None else out.view(B * Nq, Hq, D),
+                            out_dtype=out_dtype, workspace=workspace, stream=stream,
+                            quant_flags=quant_flags)
+        return o.view(B, Nq, Hq, D)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _dev(t, n)
     B, Nq, Hq, D = q.shape
@@ -117,8 +141,12 @@ def attn_fwd(q, k, v, causal=False, sm_scale=0.0, out=None, out_dtype=None, work
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, causal=False,
-                    sm_scale=0.0, out=None, out_dtype=None, workspace=None, stream=None):
-    """Packed variable-length form: q [total_q, Hq, D], k/v [total_kv, Hkv, D], cu_seqlens int32 (B+1)."""
+                    sm_scale=0.0, out=None, out_dtype=None, workspace=None, stream=None,
+                    quant_flags=0):
+    """Packed variable-length form: q [total_q, Hq, D], k/v [total_kv, Hkv, D], cu_seqlens int32 (B+1).
+
+    Nonzero ``quant_flags`` runs :func:`prepass_varlen` with those switches, then
+    :func:`attention_varlen`, on one workspace."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (cu_seqlens_q, "cu_seqlens_q"),
                  (cu_seqlens_kv, "cu_seqlens_kv")):
         _dev(t, n)
@@ -130,6 +158,12 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, causa
     odt = q.dtype if out_dtype is None else out_dtype
     out = _out(out, (total_q, Hq, D), odt, q.device)
     ws = _ws(workspace, workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv), q.device)
+    if quant_flags:
+        prepass_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, ws, causal=causal,
+                       sm_scale=sm_scale, stream=stream, quant_flags=quant_flags)
+        attention_varlen(out, ws, cu_seqlens_q, cu_seqlens_kv, Hkv, max_nq, max_nkv, total_kv,
+                         causal=causal, sm_scale=sm_scale, stream=stream)
+        return out
     _lib.check(_lib.lib().sage2_attn_fwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _code(q.dtype), _code(out.dtype),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq, Hkv, max_nq, max_nkv, total_q, total_kv,
@@ -153,10 +187,17 @@ def attention(out, workspace, B, Hq, Hkv, Nq, Nkv, D, causal=False, sm_scale=0.0
 
 
 def prepass_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, workspace,
-                   causal=False, sm_scale=0.0, stream=None):
+                   causal=False, sm_scale=0.0, stream=None, quant_flags=0):
     total_q, Hq, D = q.shape
     total_kv, Hkv, _ = k.shape
     B = cu_seqlens_q.numel() - 1
+    if quant_flags:
+        _lib.check(_lib.lib().sage2_prepass_varlen_ex(
+            _ptr(q), _ptr(k), _ptr(v), _code(q.dtype), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B,
+            Hq, Hkv, max_nq, max_nkv, total_q, total_kv, D, int(bool(causal)), float(sm_scale),
+            int(quant_flags), _ptr(workspace), workspace.numel(), _stream(stream)),
+            "sage2_prepass_varlen_ex")
+        return
     _lib.check(_lib.lib().sage2_prepass_varlen(
         _ptr(q), _ptr(k), _ptr(v), _code(q.dtype), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq,
         Hkv, max_nq, max_nkv, total_q, total_kv, D, int(bool(causal)), float(sm_scale),

@@ -53,6 +53,7 @@ def _declare(lib):
         "sage2_prepass": ([P, P, P, i, i, i, i, i, i, i, i, f, P, sz, P], i),
         "sage2_attention": ([P, i, i, i, i, i, i, i, i, f, P, sz, P], i),
         "sage2_prepass_varlen": ([P, P, P, i, P, P, i, i, i, i, i, i, i, i, i, f, P, sz, P], i),
+        "sage2_prepass_varlen_ex": ([P, P, P, i, P, P, i, i, i, i, i, i, i, i, i, f, i, P, sz, P], i),
         "sage2_attention_varlen": ([P, i, P, P, i, i, i, i, i, i, i, i, i, f, P, sz, P], i),
         "sage2_device_status": ([P, P, ctypes.POINTER(i)], i),
         "sage2_debug_tile": ([P, P, i, i, i, i, i, i, i, i, i, f, P, sz, i, i, i, i, P, P, P, P], i),

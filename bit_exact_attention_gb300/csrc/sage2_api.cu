@@ -142,10 +142,13 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGE2_OK : SAG
 static int prepass_impl(const void *q, const void *k, const void *v, int in_dtype,
                         const int *cu_q, const int *cu_kv, int B, int Hq, int Hkv, int max_nq,
                         int max_nkv, int total_q, int total_kv, int D, int causal,
-                        float sm_scale, void *ws, size_t ws_bytes, void *stream) {
+                        float sm_scale, int quant_flags, void *ws, size_t ws_bytes,
+                        void *stream) {
   int rc = check_shapes(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
   if (in_dtype != SAGE2_FP16 && in_dtype != SAGE2_BF16) return SAGE2_EINVAL;
+  if (quant_flags & ~(SAGE2_QUANT_NO_SMOOTH_Q | SAGE2_QUANT_NO_SMOOTH_K | SAGE2_QUANT_PER_BLOCK))
+    return SAGE2_EINVAL;
   if ((total_q > 0 && (!q || !aligned16(q))) || (total_kv > 0 && (!k || !v || !aligned16(k) ||
                                                                   !aligned16(v))))
     return SAGE2_EINVAL;
@@ -156,7 +159,8 @@ static int prepass_impl(const void *q, const void *k, const void *v, int in_dtyp
     return SAGE2_EINVAL;
   if ((rc = check_ws(ws, ws_bytes, L))) return rc;
   if ((rc = check_device())) return rc;
-  return cuda_status(launch_prepass(q, k, v, in_dtype, g, L, ws, (cudaStream_t)stream));
+  return cuda_status(
+      launch_prepass(q, k, v, in_dtype, quant_flags, g, L, ws, (cudaStream_t)stream));
 }
 
 static int attention_impl(void *out, int out_dtype, int in_dtype_hint, const int *cu_q,
@@ -243,7 +247,7 @@ int sage2_prepass(const void *q, const void *k, const void *v, int in_dtype, int
                   size_t workspace_bytes, void *stream) {
   if ((long long)B * Nq >= (1LL << 31) || (long long)B * Nkv >= (1LL << 31)) return SAGE2_EINVAL;
   return prepass_impl(q, k, v, in_dtype, nullptr, nullptr, B, Hq, Hkv, Nq, Nkv, B * Nq, B * Nkv,
-                      D, causal, sm_scale, workspace, workspace_bytes, stream);
+                      D, causal, sm_scale, 0, workspace, workspace_bytes, stream);
 }
 
 int sage2_prepass_varlen(const void *q, const void *k, const void *v, int in_dtype,
@@ -253,7 +257,18 @@ int sage2_prepass_varlen(const void *q, const void *k, const void *v, int in_dty
                          void *stream) {
   if (!cu_seqlens_q || !cu_seqlens_kv) return SAGE2_EINVAL;
   return prepass_impl(q, k, v, in_dtype, cu_seqlens_q, cu_seqlens_kv, B, Hq, Hkv, max_Nq,
-                      max_Nkv, total_q, total_kv, D, causal, sm_scale, workspace,
+                      max_Nkv, total_q, total_kv, D, causal, sm_scale, 0, workspace,
+                      workspace_bytes, stream);
+}
+
+int sage2_prepass_varlen_ex(const void *q, const void *k, const void *v, int in_dtype,
+                            const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq,
+                            int Hkv, int max_Nq, int max_Nkv, int total_q, int total_kv, int D,
+                            int causal, float sm_scale, int quant_flags, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  if (!cu_seqlens_q || !cu_seqlens_kv) return SAGE2_EINVAL;
+  return prepass_impl(q, k, v, in_dtype, cu_seqlens_q, cu_seqlens_kv, B, Hq, Hkv, max_Nq,
+                      max_Nkv, total_q, total_kv, D, causal, sm_scale, quant_flags, workspace,
                       workspace_bytes, stream);
 }
 

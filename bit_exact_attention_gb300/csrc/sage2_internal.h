@@ -92,7 +92,8 @@ __host__ __device__ inline int kv_tiles_for(int qt, int nq, int nkv, int causal)
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
-                           const Geometry &g, const Layout &L, void *ws, cudaStream_t st);
+                           int quant_flags, const Geometry &g, const Layout &L, void *ws,
+                           cudaStream_t st);
 
 struct AttnDebug {
   int b, h, qt, kt;        // the single work unit to run (debug launches only)

@@ -17,6 +17,10 @@
 //      order (register-blocked tiles), stored pre-multiplied by c = log2(e) * sm_scale.
 // Every padded position (channels D0..Dp, tokens past a sequence end up to its 128-row
 // boundary) is written with zero codes and zero scales.
+// Ablation switches (sage2_quant_flags) change only what these kernels write: a zero K
+// channel mean (kv_stats_final), a zero Q block mean (q_quant), or one INT4 scale per 128-key
+// K tile (k_quant) and per 128-row Q block (q_quant), still stored per 32-key group and per
+// row so that the attention kernel reads them unchanged.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -29,6 +33,7 @@ namespace {
 struct PrepassArgs {
   const uint16_t *q, *k, *v;
   int bf16;
+  int flags;  // sage2_quant_flags
   Geometry g;
   Layout L;
   WsPtrs w;
@@ -137,7 +142,7 @@ __global__ void kv_stats_final(PrepassArgs a) {
       sum += a.w.kpart[po];
       amax = fmaxf(amax, a.w.vpart[po]);
     }
-    mean = (float)(sum / (double)s.nkv);
+    mean = (a.flags & SAGE2_QUANT_NO_SMOOTH_K) ? 0.f : (float)(sum / (double)s.nkv);
   }
   a.w.kmean[o] = mean;
   a.w.vscale[o] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
@@ -146,7 +151,8 @@ __global__ void kv_stats_final(PrepassArgs a) {
 
 // ------------------------------------------------------------------ 2. K codes
 // grid (ceil(max_nkv / 128), Hkv, B), block 128: warp w quantizes the 32-token group
-// 4 * tile + w; lane l holds channels [l * CPL, l * CPL + CPL).
+// 4 * tile + w; lane l holds channels [l * CPL, l * CPL + CPL). Per-block switch: the four
+// warps share the tile's absolute maximum.
 template <int DP>
 __global__ void __launch_bounds__(128) k_quant(PrepassArgs a) {
   constexpr int CPL = DP / 32;
@@ -194,6 +200,13 @@ __global__ void __launch_bounds__(128) k_quant(PrepassArgs a) {
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (a.flags & SAGE2_QUANT_PER_BLOCK) {  // block-uniform branch
+    __shared__ float wmax[kBKV / kGK];
+    if (lane == 0) wmax[warp] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kBKV / kGK; ++w) amax = fmaxf(amax, wmax[w]);
+  }
   const float inv = amax > 0.f ? __fdiv_rn(7.f, amax) : 0.f;
   const float scale = amax > 0.f ? __fdiv_rn(amax, 7.f) : 0.f;
   uint8_t *dst = a.w.kcode + ((size_t)h * a.L.Tkv + s.kvpad0 + g0) * DP + c0;
@@ -313,7 +326,8 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
   __syncthreads();
   for (int d = tid; d < DP; d += blockDim.x) {
     const double sum = colsum[0][d] + colsum[1][d];
-    const float m = (nvalid > 0 && d < g.D0) ? (float)(sum / (double)nvalid) : 0.f;
+    const bool smooth = !(a.flags & SAGE2_QUANT_NO_SMOOTH_Q);
+    const float m = (smooth && nvalid > 0 && d < g.D0) ? (float)(sum / (double)nvalid) : 0.f;
     qbar[d] = m;
     a.w.qmean[((size_t)h * a.L.nqblk + s.qpad0 / kBQ + qb) * DP + d] = m;
   }
@@ -338,6 +352,19 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
   for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
     for (int r = 0; r < RPW; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], off));
+  if (a.flags & SAGE2_QUANT_PER_BLOCK) {  // block-uniform branch: one scale for the valid rows
+    __shared__ float wmax[kBQ / RPW];
+    float m = 0.f;
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) m = fmaxf(m, amax[r]);
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+    m = 0.f;
+#pragma unroll
+    for (int w = 0; w < kBQ / RPW; ++w) m = fmaxf(m, wmax[w]);
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) amax[r] = rbase + r < nvalid ? m : 0.f;
+  }
   const size_t row0 = (size_t)h * a.L.Tq + s.qpad0 + qb * kBQ + rbase;
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
@@ -487,12 +514,14 @@ __global__ void __launch_bounds__(256) delta_s(PrepassArgs a) {
 }  // namespace
 
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
-                           const Geometry &g, const Layout &L, void *ws, cudaStream_t st) {
+                           int quant_flags, const Geometry &g, const Layout &L, void *ws,
+                           cudaStream_t st) {
   PrepassArgs a;
   a.q = static_cast<const uint16_t *>(q);
   a.k = static_cast<const uint16_t *>(k);
   a.v = static_cast<const uint16_t *>(v);
   a.bf16 = in_dtype == SAGE2_BF16;
+  a.flags = quant_flags;
   a.g = g;
   a.L = L;
   a.w = ws_ptrs(ws, L);

@@ -108,6 +108,27 @@ int sage2_attention_varlen(void *out, int out_dtype, const int *cu_seqlens_q,
                            float sm_scale, const void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/* Quantization switches for sage2_prepass_varlen_ex: accuracy ablations of the method's
+ * three repairs (SageAttention2 research note, components 1 and 2; PMLR v267 zhang25ae,
+ * Abstract: smoothing Q, smoothing K, per-thread instead of per-block INT4 scales).
+ * 0 is the method itself. The attention kernel is the same for every setting; only what the
+ * prepass writes into the workspace changes. */
+typedef enum {
+  SAGE2_QUANT_NO_SMOOTH_Q = 1, /* Q block mean taken as 0: Q~ = Q and DeltaS = 0 */
+  SAGE2_QUANT_NO_SMOOTH_K = 2, /* K channel mean taken as 0: K~ = K */
+  SAGE2_QUANT_PER_BLOCK = 4    /* one INT4 scale per 128-row Q block and per 128-key K block
+                                  (instead of one per query row and per 32 keys) */
+} sage2_quant_flags;
+
+/* sage2_prepass_varlen with quantization switches (an OR of sage2_quant_flags; other bits
+ * return SAGE2_EINVAL). Same arguments, workspace contents and errors otherwise; follow it
+ * with sage2_attention_varlen on the same workspace. */
+int sage2_prepass_varlen_ex(const void *q, const void *k, const void *v, int in_dtype,
+                            const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq,
+                            int Hkv, int max_Nq, int max_Nkv, int total_q, int total_kv, int D,
+                            int causal, float sm_scale, int quant_flags, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
 /* Synchronizes `stream`, then reads the workspace's device status word (cleared by every
  * prepass). Returns SAGE2_OK, SAGE2_EDEVICE_TIMEOUT (a bounded wait expired) or
  * SAGE2_EINVAL (a varlen sequence exceeded max_Nq/max_Nkv); *raw (if not NULL) receives

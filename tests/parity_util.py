@@ -33,6 +33,22 @@ def metrics(a: np.ndarray, r: np.ndarray) -> dict:
             "maxabs": float(np.abs(a - r).max()) if a.size else 0.0, "cos": cos}
 
 
+def c32_of(w: W.Workload, sm_scale=0.0):
+    """c = fl32(log2(e) * fl32(sm_scale)), sm_scale defaulting to 1/sqrt(D0)."""
+    s = np.float32(sm_scale) if sm_scale > 0 else np.float32(1.0 / math.sqrt(w.d))
+    return np.float32(1.4426950408889634 * float(s))
+
+
+def kv_tiles(qt, nq, nkv, causal):
+    """KV tiles of 128 keys that Q block qt visits (bottom-right causal alignment)."""
+    nt = (nkv + 127) // 128
+    if not causal:
+        return nt
+    i_last = min(qt * 128 + 127, nq - 1)
+    j_max = i_last + (nkv - nq)
+    return 0 if j_max < 0 else min(nt, j_max // 128 + 1)
+
+
 def e4m3_to_int(u8: torch.Tensor) -> np.ndarray:
     return u8.contiguous().view(torch.float8_e4m3fn).to(torch.float32).cpu().numpy().astype(np.int64)
 
@@ -44,8 +60,9 @@ def e4m3_to_f64(u8: torch.Tensor) -> np.ndarray:
 class GpuRun:
     """Inputs on the GPU plus a workspace; prepass / attention / debug hooks."""
 
-    def __init__(self, w: W.Workload, x: dict, causal=None, sm_scale=0.0):
+    def __init__(self, w: W.Workload, x: dict, causal=None, sm_scale=0.0, quant_flags=0):
         self.w, self.x = w, x
+        self.quant_flags = quant_flags
         self.causal = w.causal if causal is None else causal
         self.sm_scale = sm_scale
         self.B = w.batch
@@ -63,7 +80,8 @@ class GpuRun:
 
     def prepass(self):
         S.prepass_varlen(self.q, self.k, self.v, self.cu_q, self.cu_kv, self.max_nq,
-                         self.max_nkv, self.ws, causal=self.causal, sm_scale=self.sm_scale)
+                         self.max_nkv, self.ws, causal=self.causal, sm_scale=self.sm_scale,
+                         quant_flags=self.quant_flags)
 
     def attention(self, out_dtype=torch.float32):
         out = torch.empty(self.tq, self.w.hq, self.w.d, dtype=out_dtype, device="cuda")
@@ -74,7 +92,8 @@ class GpuRun:
     def forward(self, out_dtype=None):
         return S.attn_fwd_varlen(self.q, self.k, self.v, self.cu_q, self.cu_kv, self.max_nq,
                                  self.max_nkv, causal=self.causal, sm_scale=self.sm_scale,
-                                 out_dtype=out_dtype, workspace=self.ws)
+                                 out_dtype=out_dtype, workspace=self.ws,
+                                 quant_flags=self.quant_flags)
 
     def status(self):
         return S.device_status(self.ws)

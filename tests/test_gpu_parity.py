@@ -9,7 +9,6 @@ Against exact FP64 attention (Mode E) the GPU must be as accurate as the emulati
 """
 from __future__ import annotations
 
-import math
 
 import numpy as np
 import pytest
@@ -18,7 +17,8 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import GpuRun, bits, e4m3_to_f64, metrics, pad_starts, unit_rows, units_sample
+from parity_util import (GpuRun, bits, c32_of, e4m3_to_f64, kv_tiles, metrics, pad_starts,
+                         unit_rows, units_sample)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,11 +32,6 @@ def _need_gpu():
     assert (major, minor) == (10, 3), f"expected an sm_103 GPU, got sm_{major}{minor}"
     oracle.build()
     S.load_library()
-
-
-def c32_of(w, sm_scale=0.0):
-    s = np.float32(sm_scale) if sm_scale > 0 else np.float32(1.0 / math.sqrt(w.d))
-    return np.float32(1.4426950408889634 * float(s))
 
 
 # Scaled workloads: the oracle finishes each in seconds; each spans several tiles and a
@@ -92,7 +87,6 @@ def test_prepass_bit_exact(name):
     # Q block means and DeltaS * c for every (q head, Q block, visited KV tile)
     qp, kp = pad_starts(x["cu_q"]), pad_starts(x["cu_kv"])
     c32 = c32_of(w)
-    from bit_exact_attention_gb300 import workloads as _  # noqa: F401
     for b in range(w.batch):
         nqb = (w.nq[b] + 127) // 128
         for h in range(w.hq):
@@ -101,19 +95,10 @@ def test_prepass_bit_exact(name):
                 np.testing.assert_array_equal(got["qmean"][h, blk], qmean[b, h, qb])
                 ds = oracle.delta_s(bits(x["k"]), dt, x["cu_kv"], b, w.hkv, h // (w.hq // w.hkv),
                                     w.d, kmean, qmean[b, h, qb])
-                ntiles = _kv_tiles(qb, w.nq[b], w.nkv[b], w.causal)
+                ntiles = kv_tiles(qb, w.nq[b], w.nkv[b], w.causal)
                 n = min(w.nkv[b], ntiles * 128)
                 want = (ds[:n] * c32).astype(np.float32)
                 np.testing.assert_array_equal(got["dsc"][h, blk, :n], want, err_msg=f"{b},{h},{qb}")
-
-
-def _kv_tiles(qt, nq, nkv, causal):
-    nt = (nkv + 127) // 128
-    if not causal:
-        return nt
-    i_last = min(qt * 128 + 127, nq - 1)
-    j_max = i_last + (nkv - nq)
-    return 0 if j_max < 0 else min(nt, j_max // 128 + 1)
 
 
 # ------------------------------------------------------------------ integer accumulators
@@ -134,7 +119,7 @@ def test_qk_accumulators_bit_exact_and_pv_partial(name):
         for (h, qt) in {(0, 0), (w.hq - 1, nqb - 1), (w.hq // 2, nqb // 2)}:
             if nqb == 0:
                 continue
-            T = _kv_tiles(qt, w.nq[b], w.nkv[b], w.causal)
+            T = kv_tiles(qt, w.nq[b], w.nkv[b], w.causal)
             for kt in sorted({0, T - 1}):
                 if kt < 0:
                     continue
