@@ -38,6 +38,11 @@ METRIC = "attention TOPS (4BHNqNkvD/t) at N=8k-32k, D=128; % of GB300 dense INT8
 WORKLOADS = {w.name: w for w in W.ALL}
 WORKLOADS.update({"gqa_long": W.GQA_LONG, "prefill": W.PREFILL, "video_dit": W.VIDEO_DIT,
                   "varlen": W.VARLEN, "tiny": W.TINY})
+# head-dim sweep: the LLM prefill shape at other head dims (D0 not a multiple of 64 runs padded
+# to 64 or 128 channels; the metric counts D0)
+WORKLOADS.update({f"prefill_d{d}": W.scaled(W.PREFILL, W.PREFILL.nq, W.PREFILL.nkv, d=d,
+                                             name=f"llm_prefill_causal_B2_H32_N4096_D{d}_bf16")
+                  for d in (32, 64, 80, 96, 112)})
 FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor ratio (GB300)
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # DRAM bytes (read + write) of one attention launch, from a one-pass ncu capture of

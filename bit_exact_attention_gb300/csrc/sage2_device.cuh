@@ -335,6 +335,20 @@ __device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, f
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -410,6 +424,21 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
   s = __fadd_rn(a, b);
   const float bb = __fsub_rn(s, a);
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// Two double-float accumulators at once: (hi_i, lo_i) += x_i, i = 0, 1, each lane the same
+// operation sequence as df_add.
+__device__ __forceinline__ void df_add2(float &hi0, float &hi1, float &lo0, float &lo1, float x0,
+                                        float x1) {
+  float s0, s1, bb0, bb1, t0, t1, u0, u1, v0, v1, e0, e1;
+  add2(s0, s1, hi0, hi1, x0, x1);
+  sub2(bb0, bb1, s0, s1, hi0, hi1);
+  sub2(t0, t1, s0, s1, bb0, bb1);
+  sub2(u0, u1, hi0, hi1, t0, t1);
+  sub2(v0, v1, x0, x1, bb0, bb1);
+  add2(e0, e1, u0, u1, v0, v1);
+  add2(lo0, lo1, lo0, lo1, e0, e1);
+  hi0 = s0;
+  hi1 = s1;
 }
 // Double-float accumulator: (hi, lo) += x.
 __device__ __forceinline__ void df_add(float &hi, float &lo, float x) {

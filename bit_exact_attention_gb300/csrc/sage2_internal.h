@@ -12,7 +12,7 @@ namespace sage2 {
 constexpr int kBQ = 128;        // Q tile rows = Q smoothing block
 constexpr int kBKV = 128;       // KV tile keys = online-softmax step = two-level partial
 constexpr int kGK = 32;         // K tokens per INT4 scale group
-constexpr int kStatChunk = 64;  // tokens per partial in the K/V statistics pass
+constexpr int kStatChunk = 32;  // tokens per partial in the K/V statistics pass
 
 // Problem geometry. Dense calls have cu_q == cu_kv == nullptr and every sequence of length
 // max_nq / max_nkv; varlen calls pass device prefix sums.

@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "sage2_device.cuh"
 #include "sage2_internal.h"
 
@@ -32,25 +34,37 @@ namespace {
 
 struct PrepassArgs {
   const uint16_t *q, *k, *v;
-  int bf16;
   int flags;  // sage2_quant_flags
   Geometry g;
   Layout L;
   WsPtrs w;
 };
 
-__device__ __forceinline__ float to_f32(uint16_t bits, int bf16) {
-  if (bf16) return __uint_as_float(((uint32_t)bits) << 16);
+template <bool BF16>
+__device__ __forceinline__ float to_f32(uint16_t bits) {
+  if (BF16) return __uint_as_float(((uint32_t)bits) << 16);
   return __half2float(__ushort_as_half(bits));
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &u, int bf16, float (&x)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = to_f32((uint16_t)(w[i] & 0xFFFFu), bf16);
-    x[2 * i + 1] = to_f32((uint16_t)(w[i] >> 16), bf16);
+// The two 16-bit values of a 32-bit word (low half first) as floats.
+template <bool BF16>
+__device__ __forceinline__ void unpack2(uint32_t w, float &x0, float &x1) {
+  if (BF16) {
+    x0 = __uint_as_float(w << 16);
+    x1 = __uint_as_float(w & 0xFFFF0000u);
+  } else {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    x0 = f.x;
+    x1 = f.y;
   }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
+  unpack2<BF16>(u.x, x[0], x[1]);
+  unpack2<BF16>(u.y, x[2], x[3]);
+  unpack2<BF16>(u.z, x[4], x[5]);
+  unpack2<BF16>(u.w, x[6], x[7]);
 }
 
 // INT4-grid code of x * inv, as an e4m3 byte (canonical +0 for zero).
@@ -65,14 +79,16 @@ __device__ __forceinline__ void flag_bad_seq(int *status) {
 }
 
 // ------------------------------------------------------------------ 1a. K/V statistics
-// grid (nchunk, B), block = 32 * ceil(Hkv * D0 / 8 / 32) capped at 256. Each thread owns a
+// grid (nchunk, B, ceil(Hkv * D0 / 8 / kStatThreads)), block kStatThreads. Each thread owns a
 // run of 8 channels (one 16-byte vector of a token row) and walks kStatChunk tokens.
-__global__ void __launch_bounds__(256) kv_stats_partial(PrepassArgs a) {
+constexpr int kStatThreads = 128;
+template <bool BF16>
+__global__ void __launch_bounds__(kStatThreads) kv_stats_partial(PrepassArgs a) {
   const int b = blockIdx.y, chunk = blockIdx.x;
   const Geometry &g = a.g;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
   if (!s.ok) {
-    if (threadIdx.x == 0 && chunk == 0) flag_bad_seq(a.w.status);
+    if (threadIdx.x == 0 && chunk == 0 && blockIdx.z == 0) flag_bad_seq(a.w.status);
     return;
   }
   const int t0 = chunk * kStatChunk;
@@ -80,41 +96,36 @@ __global__ void __launch_bounds__(256) kv_stats_partial(PrepassArgs a) {
   const int t1 = min(t0 + kStatChunk, s.nkv);
   const int row_elems = g.Hkv * g.D0;
   const int nvec = row_elems / 8;
-  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+  {
+    const int vi = blockIdx.z * kStatThreads + threadIdx.x;
+    if (vi >= nvec) return;
     float hi[8], lo[8], mx[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) hi[e] = lo[e] = mx[e] = 0.f;
     const uint4 *kp = reinterpret_cast<const uint4 *>(a.k + (size_t)(s.kv0 + t0) * row_elems) + vi;
     const uint4 *vp = reinterpret_cast<const uint4 *>(a.v + (size_t)(s.kv0 + t0) * row_elems) + vi;
     const int stride = nvec;
-    int t = t0;
-    for (; t + 4 <= t1; t += 4) {
-      uint4 kk[4], vv[4];
+    constexpr int U = 8;  // tokens whose loads are all issued before any is used
+#pragma unroll 1
+    for (int t = t0; t < t1; t += U) {
+      uint4 kk[U], vv[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        kk[u] = __ldg(kp + (size_t)(t - t0 + u) * stride);
-        vv[u] = __ldg(vp + (size_t)(t - t0 + u) * stride);
+      for (int u = 0; u < U; ++u) {  // tokens past the end read as 0 and add nothing
+        const bool ok = t + u < t1;
+        kk[u] = ok ? __ldg(kp + (size_t)(t - t0 + u) * stride) : make_uint4(0u, 0u, 0u, 0u);
+        vv[u] = ok ? __ldg(vp + (size_t)(t - t0 + u) * stride) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {  // tokens in order
+      for (int u = 0; u < U; ++u) {  // tokens in order
         float xk[8], xv[8];
-        unpack8(kk[u], a.bf16, xk);
-        unpack8(vv[u], a.bf16, xv);
+        unpack8<BF16>(kk[u], xk);
+        unpack8<BF16>(vv[u], xv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          df_add(hi[e], lo[e], xk[e]);
+        for (int e = 0; e < 8; e += 2) {
+          df_add2(hi[e], hi[e + 1], lo[e], lo[e + 1], xk[e], xk[e + 1]);
           mx[e] = fmaxf(mx[e], fabsf(xv[e]));
+          mx[e + 1] = fmaxf(mx[e + 1], fabsf(xv[e + 1]));
         }
-      }
-    }
-    for (; t < t1; ++t) {
-      float xk[8], xv[8];
-      unpack8(__ldg(kp + (size_t)(t - t0) * stride), a.bf16, xk);
-      unpack8(__ldg(vp + (size_t)(t - t0) * stride), a.bf16, xv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        df_add(hi[e], lo[e], xk[e]);
-        mx[e] = fmaxf(mx[e], fabsf(xv[e]));
       }
     }
     const size_t o = ((size_t)b * a.L.nchunk + chunk) * row_elems + (size_t)vi * 8;
@@ -126,161 +137,183 @@ __global__ void __launch_bounds__(256) kv_stats_partial(PrepassArgs a) {
   }
 }
 
-// grid (B * Hkv), block Dp.
-__global__ void kv_stats_final(PrepassArgs a) {
+// grid (B * Hkv, Dp / 32), block 1024 = 32 channels x 32 parts: part p sums chunks p, p + 32,
+// ... in FP64, then the parts are added in order. The chunk sums are exact (see above), and so
+// is every FP64 sum of them for 16-bit inputs, so the order does not change the result.
+constexpr int kFinalThreads = 1024, kFinalChan = 32, kFinalParts = kFinalThreads / kFinalChan;
+__global__ void __launch_bounds__(kFinalThreads) kv_stats_final(PrepassArgs a) {
+  __shared__ double psum[kFinalParts][kFinalChan];
+  __shared__ float pmax[kFinalParts][kFinalChan];
   const Geometry &g = a.g;
-  const int b = blockIdx.x / g.Hkv, h = blockIdx.x % g.Hkv, d = threadIdx.x;
+  const int b = blockIdx.x / g.Hkv, h = blockIdx.x % g.Hkv;
+  const int dl = threadIdx.x % kFinalChan, part = threadIdx.x / kFinalChan;
+  const int d = blockIdx.y * kFinalChan + dl;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
-  const size_t o = ((size_t)b * g.Hkv + h) * g.Dp + d;
-  float mean = 0.f, amax = 0.f;
+  double sum = 0.0;
+  float amax = 0.f;
   if (s.ok && d < g.D0 && s.nkv > 0) {
     const int nch = (s.nkv + kStatChunk - 1) / kStatChunk;
     const int row_elems = g.Hkv * g.D0;
-    double sum = 0.0;
-    for (int c = 0; c < nch; ++c) {
+#pragma unroll 4
+    for (int c = part; c < nch; c += kFinalParts) {
       const size_t po = ((size_t)b * a.L.nchunk + c) * row_elems + (size_t)h * g.D0 + d;
       sum += a.w.kpart[po];
       amax = fmaxf(amax, a.w.vpart[po]);
     }
-    mean = (a.flags & SAGE2_QUANT_NO_SMOOTH_K) ? 0.f : (float)(sum / (double)s.nkv);
   }
+  psum[part][dl] = sum;
+  pmax[part][dl] = amax;
+  __syncthreads();
+  if (part != 0) return;
+  for (int p = 1; p < kFinalParts; ++p) {
+    sum += psum[p][dl];
+    amax = fmaxf(amax, pmax[p][dl]);
+  }
+  const size_t o = ((size_t)b * g.Hkv + h) * g.Dp + d;
+  float mean = 0.f;
+  if (s.ok && d < g.D0 && s.nkv > 0)
+    mean = (a.flags & SAGE2_QUANT_NO_SMOOTH_K) ? 0.f : (float)(sum / (double)s.nkv);
   a.w.kmean[o] = mean;
   a.w.vscale[o] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
   a.w.vinv[o] = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
 }
 
 // ------------------------------------------------------------------ 2. K codes
-// grid (ceil(max_nkv / 128), Hkv, B), block 128: warp w quantizes the 32-token group
-// 4 * tile + w; lane l holds channels [l * CPL, l * CPL + CPL). Per-block switch: the four
-// warps share the tile's absolute maximum.
-template <int DP>
-__global__ void __launch_bounds__(128) k_quant(PrepassArgs a) {
-  constexpr int CPL = DP / 32;
+// grid (ceil(max_nkv / 128), Hkv, B), block 256. The tile's 128 x D0 keys are staged in shared
+// memory with asynchronous 16-byte copies (rows past the end and channels past D0 read as 0);
+// warp w handles keys 16w .. 16w + 15, i.e. half of the 32-key scale group w / 2; lane l
+// channels [l * CPL, l * CPL + CPL). Per-block switch: the eight warps share one maximum.
+template <int DP, bool BF16>
+__global__ void __launch_bounds__(256) k_quant(PrepassArgs a) {
+  constexpr int CPL = DP / 32, RPW = 16;
+  __shared__ __align__(16) uint16_t blk[kBKV][DP];
+  __shared__ float wmax[kBKV / RPW];
+  const Geometry &g = a.g;
+  const int b = blockIdx.z, h = blockIdx.y, tile = blockIdx.x;
+  const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
+  if (!s.ok || tile * kBKV >= ((s.nkv + kBKV - 1) / kBKV) * kBKV) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t row_elems = (size_t)g.Hkv * g.D0;
+  const int nvalid = min(kBKV, s.nkv - tile * kBKV);
+  constexpr int kChunks = DP / 8;
+  for (int c = tid; c < kBKV * kChunks; c += blockDim.x) {
+    const int r = c / kChunks, ch = (c % kChunks) * 8;
+    uint16_t *dst = &blk[r][ch];
+    if (r < nvalid && ch < g.D0) {
+      const uint16_t *src = a.k + (size_t)(s.kv0 + tile * kBKV + r) * row_elems + (size_t)h * g.D0 + ch;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                   : "memory");
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const int c0 = lane * CPL;
+  const bool chan_ok = c0 < g.D0;  // D0 % 8 == 0, so a lane's channels are all in or all out
+  float mu[CPL];
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) mu[e] = a.w.kmean[((size_t)b * g.Hkv + h) * DP + c0 + e];
+  const int rbase = warp * RPW;
+  auto smoothed = [&](int r, int e) {  // K~ = fl32(K - kmean); 0 outside the data
+    return (rbase + r < nvalid && chan_ok) ? __fsub_rn(to_f32<BF16>(blk[rbase + r][c0 + e]), mu[e])
+                                           : 0.f;
+  };
+  float amax = 0.f;
+#pragma unroll
+  for (int r = 0; r < RPW; ++r)
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) amax = fmaxf(amax, fabsf(smoothed(r, e)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (lane == 0) wmax[warp] = amax;
+  __syncthreads();
+  if (a.flags & SAGE2_QUANT_PER_BLOCK) {
+#pragma unroll
+    for (int w = 0; w < kBKV / RPW; ++w) amax = fmaxf(amax, wmax[w]);
+  } else {
+    amax = fmaxf(wmax[warp & ~1], wmax[warp | 1]);  // the two halves of the 32-key group
+  }
+  const float inv = amax > 0.f ? __fdiv_rn(7.f, amax) : 0.f;
+  const float scale = amax > 0.f ? __fdiv_rn(amax, 7.f) : 0.f;
+  uint8_t *dst = a.w.kcode + ((size_t)h * a.L.Tkv + s.kvpad0 + tile * kBKV + rbase) * DP + c0;
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    if (CPL == 4) {
+      const uint32_t lo = cvt_e4m3x2(int4_code(smoothed(r, 0), inv), int4_code(smoothed(r, 1), inv));
+      const uint32_t hi = cvt_e4m3x2(int4_code(smoothed(r, 2), inv), int4_code(smoothed(r, 3), inv));
+      *reinterpret_cast<uint32_t *>(dst + (size_t)r * DP) = lo | (hi << 16);
+    } else {
+      *reinterpret_cast<uint16_t *>(dst + (size_t)r * DP) =
+          (uint16_t)cvt_e4m3x2(int4_code(smoothed(r, 0), inv), int4_code(smoothed(r, 1), inv));
+    }
+  }
+  if (lane == 0 && (warp & 1) == 0)
+    a.w.kscale[(size_t)h * (a.L.Tkv / kGK) + (s.kvpad0 + tile * kBKV) / kGK + warp / 2] = scale;
+}
+
+// ------------------------------------------------------------------ 3. V codes, transposed
+// grid (ceil(max_nkv / 128), Hkv, B), block 256. Warp w covers 64 channels (channel group
+// w % CG, CG = DP / 64) of TPW = 128 / (8 / CG) consecutive tokens (token group w / CG); lane l
+// owns channels 2l, 2l + 1 of the group. Each token row is one 128-byte load per warp; each
+// lane writes TPW contiguous code bytes per channel (whole 16- or 32-byte pieces of the
+// transposed rows), so no shared-memory transpose is needed.
+template <int DP, bool BF16>
+__global__ void __launch_bounds__(256) v_quant(PrepassArgs a) {
+  constexpr int CG = DP / 64, TG = 8 / CG, TPW = kBKV / TG, WORDS = TPW / 4;
   const Geometry &g = a.g;
   const int b = blockIdx.z, h = blockIdx.y, tile = blockIdx.x;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
   if (!s.ok || tile * kBKV >= ((s.nkv + kBKV - 1) / kBKV) * kBKV) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c0 = lane * CPL;
-  const bool chan_ok = c0 < g.D0;  // D0 % 8 == 0, so a lane's channels are all in or all out
-  const int g0 = tile * kBKV + warp * kGK;  // first token of this group (sequence-local)
-  float mu[CPL];
-#pragma unroll
-  for (int e = 0; e < CPL; ++e) mu[e] = a.w.kmean[((size_t)b * g.Hkv + h) * DP + c0 + e];
-  float x[kGK][CPL];
-  float amax = 0.f;
+  const int c = 64 * (warp % CG) + 2 * lane;
+  const int t0 = tile * kBKV + TPW * (warp / CG);  // sequence-local first token
+  const bool chan_ok = c < g.D0;                  // D0 even: both channels in or out
+  const size_t vo = ((size_t)b * g.Hkv + h) * DP + c;
+  const float inv0 = a.w.vinv[vo], inv1 = a.w.vinv[vo + 1];
   const size_t row_elems = (size_t)g.Hkv * g.D0;
+  const uint16_t *src = a.v + (size_t)(s.kv0 + t0) * row_elems + (size_t)h * g.D0 + c;
+  uint32_t raw[TPW];
 #pragma unroll
-  for (int r = 0; r < kGK; ++r) {
-    const int t = g0 + r;
-    float val[CPL];
+  for (int u = 0; u < TPW; ++u)
+    raw[u] = (chan_ok && t0 + u < s.nkv) ? __ldg(reinterpret_cast<const uint32_t *>(src + (size_t)u * row_elems))
+                                         : 0u;
+  uint32_t w0[WORDS], w1[WORDS];
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) val[e] = 0.f;
-    if (t < s.nkv && chan_ok) {
-      const uint16_t *src = a.k + (size_t)(s.kv0 + t) * row_elems + (size_t)h * g.D0 + c0;
-      if (CPL == 4) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(src));
-        val[0] = to_f32((uint16_t)(u.x & 0xFFFFu), a.bf16);
-        val[1] = to_f32((uint16_t)(u.x >> 16), a.bf16);
-        val[2] = to_f32((uint16_t)(u.y & 0xFFFFu), a.bf16);
-        val[3] = to_f32((uint16_t)(u.y >> 16), a.bf16);
-      } else {
-        const uint32_t u = __ldg(reinterpret_cast<const uint32_t *>(src));
-        val[0] = to_f32((uint16_t)(u & 0xFFFFu), a.bf16);
-        val[1] = to_f32((uint16_t)(u >> 16), a.bf16);
-      }
+  for (int i = 0; i < WORDS; ++i) w0[i] = w1[i] = 0u;
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) {
-        val[e] = __fsub_rn(val[e], mu[e]);
-        amax = fmaxf(amax, fabsf(val[e]));
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < CPL; ++e) x[r][e] = val[e];
+  for (int u = 0; u < TPW; ++u) {
+    float x0, x1;
+    unpack2<BF16>(raw[u], x0, x1);
+    const uint32_t two = cvt_e4m3x2(__fmul_rn(x0, inv0), __fmul_rn(x1, inv1));
+    w0[u / 4] |= (two & 0xFFu) << (8 * (u % 4));
+    w1[u / 4] |= ((two >> 8) & 0xFFu) << (8 * (u % 4));
   }
+  uint8_t *d0 = a.w.vcodeT + ((size_t)h * DP + c) * a.L.Tkv + s.kvpad0 + t0;
+  uint8_t *d1 = d0 + a.L.Tkv;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  if (a.flags & SAGE2_QUANT_PER_BLOCK) {  // block-uniform branch
-    __shared__ float wmax[kBKV / kGK];
-    if (lane == 0) wmax[warp] = amax;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < kBKV / kGK; ++w) amax = fmaxf(amax, wmax[w]);
-  }
-  const float inv = amax > 0.f ? __fdiv_rn(7.f, amax) : 0.f;
-  const float scale = amax > 0.f ? __fdiv_rn(amax, 7.f) : 0.f;
-  uint8_t *dst = a.w.kcode + ((size_t)h * a.L.Tkv + s.kvpad0 + g0) * DP + c0;
-#pragma unroll
-  for (int r = 0; r < kGK; ++r) {
-    if (CPL == 4) {
-      const uint32_t lo = cvt_e4m3x2(int4_code(x[r][0], inv), int4_code(x[r][1], inv));
-      const uint32_t hi = cvt_e4m3x2(int4_code(x[r][2], inv), int4_code(x[r][3], inv));
-      *reinterpret_cast<uint32_t *>(dst + (size_t)r * DP) = lo | (hi << 16);
-    } else {
-      *reinterpret_cast<uint16_t *>(dst + (size_t)r * DP) =
-          (uint16_t)cvt_e4m3x2(int4_code(x[r][0], inv), int4_code(x[r][1], inv));
-    }
-  }
-  if (lane == 0) a.w.kscale[(size_t)h * (a.L.Tkv / kGK) + (s.kvpad0 + g0) / kGK] = scale;
-}
-
-// ------------------------------------------------------------------ 3. V codes, transposed
-// grid (ceil(max_nkv / 128), Hkv, B), block 256.
-template <int DP>
-__global__ void __launch_bounds__(256) v_quant(PrepassArgs a) {
-  constexpr int TP = kBKV + 16;  // padded smem row (bytes)
-  __shared__ __align__(16) uint8_t tb[DP * TP];
-  __shared__ float vinv[DP];
-  const Geometry &g = a.g;
-  const int b = blockIdx.z, h = blockIdx.y, tile = blockIdx.x;
-  const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
-  if (!s.ok || tile * kBKV >= ((s.nkv + kBKV - 1) / kBKV) * kBKV) return;
-  for (int d = threadIdx.x; d < DP; d += blockDim.x)
-    vinv[d] = a.w.vinv[((size_t)b * g.Hkv + h) * DP + d];
-  __syncthreads();
-  const size_t row_elems = (size_t)g.Hkv * g.D0;
-  constexpr int VPT = DP / 8;  // 8-channel vectors per token (padded dim)
-  for (int i = threadIdx.x; i < kBKV * VPT; i += blockDim.x) {
-    const int tok = i / VPT, c8 = (i % VPT) * 8;
-    const int t = tile * kBKV + tok;
-    float x[8];
-    if (t < s.nkv && c8 < g.D0) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a.v + (size_t)(s.kv0 + t) * row_elems +
-                                                            (size_t)h * g.D0 + c8));
-      unpack8(u, a.bf16, x);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const uint32_t two = cvt_e4m3x2(__fmul_rn(x[e], vinv[c8 + e]), __fmul_rn(x[e + 1], vinv[c8 + e + 1]));
-      tb[(c8 + e) * TP + tok] = (uint8_t)(two & 0xFF);
-      tb[(c8 + e + 1) * TP + tok] = (uint8_t)(two >> 8);
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < DP * (kBKV / 16); i += blockDim.x) {
-    const int c = i / (kBKV / 16), part = i % (kBKV / 16);
-    const uint4 val = *reinterpret_cast<const uint4 *>(&tb[c * TP + part * 16]);
-    *reinterpret_cast<uint4 *>(a.w.vcodeT + ((size_t)h * DP + c) * a.L.Tkv + s.kvpad0 +
-                               tile * kBKV + part * 16) = val;
+  for (int i = 0; i < WORDS; i += 4) {
+    *reinterpret_cast<uint4 *>(d0 + 4 * i) = make_uint4(w0[i], w0[i + 1], w0[i + 2], w0[i + 3]);
+    *reinterpret_cast<uint4 *>(d1 + 4 * i) = make_uint4(w1[i], w1[i + 1], w1[i + 2], w1[i + 3]);
   }
 }
 
 // ------------------------------------------------------------------ 4. Q codes
 // grid (ceil(max_nq / 128), Hq, B), block 256. The block's 128 x D0 input values are staged in
 // shared memory with asynchronous 16-byte copies (few registers, so many CTAs per SM keep enough
-// loads in flight). Channel sums: thread t sums channel t % DP over one half of the rows in
-// double-float; the two halves are combined in double. The sums are exact for 16-bit inputs, so
-// the mean is the definition's fl32(sum / n). Quantization: warp w owns rows 16w .. 16w + 15,
-// lane l channels [l * CPL, l * CPL + CPL).
-template <int DP>
+// loads in flight). Channel sums: thread t owns the channel pair 2 (t % (DP/2)) and one of
+// 256 / (DP/2) row ranges, summed as two double-float accumulators; the ranges are combined in
+// double. The sums are exact for 16-bit inputs, so the mean is the definition's fl32(sum / n).
+// Quantization: warp w owns rows 16w .. 16w + 15, lane l channels [l * CPL, l * CPL + CPL), all
+// elementwise steps on packed FP32 pairs (each lane of a pair rounds like the scalar form).
+template <int DP, bool BF16>
 __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
   constexpr int CPL = DP / 32, RPW = 16;
+  constexpr int kPairs = DP / 2, kParts = 256 / kPairs, kRowsPer = kBQ / kParts;
   __shared__ __align__(16) uint16_t blk[kBQ][DP];  // rows past the end / channels past D0: 0
-  __shared__ double colsum[2][DP];
+  __shared__ double colsum[kParts][DP];
   __shared__ float qbar[DP];
+  __shared__ float wmax[kBQ / RPW];
   const Geometry &g = a.g;
   const int b = blockIdx.z, h = blockIdx.y, qb = blockIdx.x;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
@@ -307,25 +340,23 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  {  // channel sums: thread t, channel t % DP, rows [half * 64, half * 64 + 64) (256 / DP halves)
-    constexpr int kParts = 256 / DP, kRowsPer = kBQ / kParts;
-    const int d = tid % DP, part = tid / DP;
-    float hi = 0.f, lo = 0.f;
+  {  // channel sums (staged zeros add nothing)
+    const int d = 2 * (tid % kPairs), part = tid / kPairs;
+    float hi0 = 0.f, hi1 = 0.f, lo0 = 0.f, lo1 = 0.f;
 #pragma unroll 8
-    for (int r = part * kRowsPer; r < (part + 1) * kRowsPer; ++r)
-      df_add(hi, lo, to_f32(blk[r][d], a.bf16));  // staged zeros add nothing
-    if (kParts == 2) {
-      colsum[part][d] = (double)hi + (double)lo;
-    } else {  // DP = 64: four parts, folded pairwise into the two slots
-      __shared__ double part4[4][64];
-      part4[part][d] = (double)hi + (double)lo;
-      __syncthreads();
-      if (part < 2) colsum[part][d] = part4[2 * part][d] + part4[2 * part + 1][d];
+    for (int r = part * kRowsPer; r < (part + 1) * kRowsPer; ++r) {
+      float x0, x1;
+      unpack2<BF16>(*reinterpret_cast<const uint32_t *>(&blk[r][d]), x0, x1);
+      df_add2(hi0, hi1, lo0, lo1, x0, x1);
     }
+    colsum[part][d] = (double)hi0 + (double)lo0;
+    colsum[part][d + 1] = (double)hi1 + (double)lo1;
   }
   __syncthreads();
   for (int d = tid; d < DP; d += blockDim.x) {
-    const double sum = colsum[0][d] + colsum[1][d];
+    double sum = colsum[0][d];
+#pragma unroll
+    for (int p = 1; p < kParts; ++p) sum += colsum[p][d];
     const bool smooth = !(a.flags & SAGE2_QUANT_NO_SMOOTH_Q);
     const float m = (smooth && nvalid > 0 && d < g.D0) ? (float)(sum / (double)nvalid) : 0.f;
     qbar[d] = m;
@@ -339,175 +370,254 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
 #pragma unroll
   for (int e = 0; e < CPL; ++e) mb[e] = qbar[c0 + e];
   const int rbase = warp * RPW;  // row within the block
+  auto smoothed = [&](int r, float (&x)[CPL]) {
+    if (rbase + r < nvalid && chan_ok) {
+      if (CPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(&blk[rbase + r][c0]);
+        unpack2<BF16>(w.x, x[0], x[1]);
+        unpack2<BF16>(w.y, x[2], x[3]);
+      } else {
+        unpack2<BF16>(*reinterpret_cast<const uint32_t *>(&blk[rbase + r][c0]), x[0], x[1]);
+      }
+#pragma unroll
+      for (int e = 0; e < CPL; e += 2) sub2(x[e], x[e + 1], x[e], x[e + 1], mb[e], mb[e + 1]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) x[e] = 0.f;
+    }
+  };
   float amax[RPW];
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
-    const bool rv = rbase + r < nvalid && chan_ok;
+    float x[CPL];
+    smoothed(r, x);
     amax[r] = 0.f;
 #pragma unroll
-    for (int e = 0; e < CPL; ++e)
-      amax[r] = fmaxf(amax[r], fabsf(rv ? __fsub_rn(to_f32(blk[rbase + r][c0 + e], a.bf16), mb[e]) : 0.f));
+    for (int e = 0; e < CPL; ++e) amax[r] = fmaxf(amax[r], fabsf(x[e]));
   }
+  // Transposing butterfly: after the steps over lane bits 4..1 lane l holds the maximum of row
+  // l >> 1 over the lanes that agree with it in those bits; the last step (bit 0) completes it.
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
+  for (int half = RPW / 2, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool upper = lane & bit;
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], off));
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? amax[i] : amax[i + half];
+      const float keep = upper ? amax[i + half] : amax[i];
+      amax[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, bit));
+    }
+  }
+  float rmax = fmaxf(amax[0], __shfl_xor_sync(0xffffffffu, amax[0], 1));  // row lane >> 1
   if (a.flags & SAGE2_QUANT_PER_BLOCK) {  // block-uniform branch: one scale for the valid rows
-    __shared__ float wmax[kBQ / RPW];
-    float m = 0.f;
+    float m = rmax;
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) m = fmaxf(m, amax[r]);
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     if (lane == 0) wmax[warp] = m;
     __syncthreads();
     m = 0.f;
 #pragma unroll
     for (int w = 0; w < kBQ / RPW; ++w) m = fmaxf(m, wmax[w]);
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) amax[r] = rbase + r < nvalid ? m : 0.f;
+    rmax = rbase + (lane >> 1) < nvalid ? m : 0.f;
   }
+  // one division per lane (row lane >> 1); rows past the end have rmax = 0: codes and scale 0
+  const float inv_mine = rmax > 0.f ? __fdiv_rn(7.f, rmax) : 0.f;
   const size_t row0 = (size_t)h * a.L.Tq + s.qpad0 + qb * kBQ + rbase;
+  if ((lane & 1) == 0) a.w.qscale[row0 + (lane >> 1)] = rmax > 0.f ? __fdiv_rn(rmax, 7.f) : 0.f;
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
-    const bool rv = rbase + r < nvalid && chan_ok;
-    float xt[CPL];
+    float x[CPL];
+    smoothed(r, x);
+    const float inv = __shfl_sync(0xffffffffu, inv_mine, 2 * r);
+    float t[CPL];
 #pragma unroll
-    for (int e = 0; e < CPL; ++e)
-      xt[e] = rv ? __fsub_rn(to_f32(blk[rbase + r][c0 + e], a.bf16), mb[e]) : 0.f;
-    const float inv = amax[r] > 0.f ? __fdiv_rn(7.f, amax[r]) : 0.f;
+    for (int e = 0; e < CPL; e += 2) mul2(t[e], t[e + 1], x[e], x[e + 1], inv, inv);
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) t[e] = rintf(t[e]);
+    // |x| <= rmax and inv = fl32(7 / rmax) give |fl32(x * inv)| <= 7 whenever inv is finite;
+    // only an overflowed inv (rmax below 7 / FLT_MAX) needs the clamp to [-7, 7]
+    if (__builtin_expect(isinf(inv), 0)) {
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) t[e] = fminf(fmaxf(t[e], -7.f), 7.f);
+    }
+#pragma unroll
+    for (int e = 0; e < CPL; e += 2) add2(t[e], t[e + 1], t[e], t[e + 1], 0.f, 0.f);  // +0 for -0
     uint8_t *dst = a.w.qcode + (row0 + r) * DP + c0;
     if (CPL == 4) {
-      const uint32_t lo2 = cvt_e4m3x2(int4_code(xt[0], inv), int4_code(xt[1], inv));
-      const uint32_t hi2 = cvt_e4m3x2(int4_code(xt[2], inv), int4_code(xt[3], inv));
-      *reinterpret_cast<uint32_t *>(dst) = lo2 | (hi2 << 16);
+      *reinterpret_cast<uint32_t *>(dst) = cvt_e4m3x2(t[0], t[1]) | (cvt_e4m3x2(t[2], t[3]) << 16);
     } else {
-      *reinterpret_cast<uint16_t *>(dst) =
-          (uint16_t)cvt_e4m3x2(int4_code(xt[0], inv), int4_code(xt[1], inv));
+      *reinterpret_cast<uint16_t *>(dst) = (uint16_t)cvt_e4m3x2(t[0], t[1]);
     }
-    if (lane == 0) a.w.qscale[row0 + r] = amax[r] > 0.f ? __fdiv_rn(amax[r], 7.f) : 0.f;
   }
 }
 
 // ------------------------------------------------------------------ 5. DeltaS
 // A small FP32 GEMM per (sequence, kv head): rows are the (Q block, q head of the group)
 // pairs, ordered Q-block-major (r = qb * g + head), columns the keys, inner dimension the
-// channels. grid (key tiles of 128, row tiles of 128, B * Hkv), block 256. Thread (tr, tk)
-// owns rows 8tr..8tr+7 and keys 8tk..8tk+7; channels are staged 32 at a time in shared memory,
-// transposed, and every output is one FMA chain in increasing channel order (the same
-// operation sequence as the definition, so the result is bit-identical to it). Causal: a
-// (row tile, key tile) pair that no row of the tile visits is skipped; rows that do not visit
-// the key tile are not written.
-constexpr int kDsRows = 128, kDsKeys = 128, kDsChan = 32;
+// channels. A CTA computes a ROWS x KEYS tile (ROWS * KEYS = 128 * 128; the launcher picks the
+// row-tile height that wastes the fewest rows, so a kv head with few (Q block, head) rows does
+// not compute a 128-row tile of padding). grid (key tiles, row tiles, B * Hkv), block 256.
+// Thread (tr, tk) owns 8 rows and the 8 keys {4tk + e, KEYS/2 + 4tk + e : e < 4} (so a warp's
+// shared-memory reads are contiguous 16-byte pieces). Channels are staged CH at a time in
+// shared memory (two buffers, one barrier per chunk), transposed, converted to FP32 and
+// smoothed; a chunk's global loads are issued two chunks ahead of its FMAs. Every output is one
+// FMA chain in increasing channel order (the same operation sequence as the definition, so the
+// result is bit-identical to it). Causal: a CTA whose rows visit none of its keys returns; a
+// warp whose rows visit none of them skips the FMAs; an output whose 128-key tile its Q block
+// does not visit is not written.
+template <int ROWS>
+struct DsTile {
+  static constexpr int kKeys = kBQ * kBKV / ROWS;  // 128, 256 or 512
+  static constexpr int kCh = ROWS == 32 ? 8 : 16;  // channels per staged chunk
+  static constexpr int kTk = kKeys / 8;            // threads along the keys
+  static constexpr int kKVec = kKeys * (kCh / 8) / 256;              // 8-channel K vectors
+  static constexpr int kQVec = (ROWS * (kCh / 4) + 255) / 256;       // 4-channel Q-mean vectors
+  static_assert(kTk * (ROWS / 8) == 256, "256 threads, 8 x 8 outputs each");
+  static_assert(kKVec * 256 == kKeys * (kCh / 8), "whole K vectors per thread");
+};
 
-template <int DP>
-__global__ void __launch_bounds__(256) delta_s(PrepassArgs a) {
-  __shared__ __align__(16) float Qs[kDsChan][kDsRows];
-  __shared__ __align__(16) float Ks[kDsChan][kDsKeys];
+template <int DP, int ROWS, bool BF16>
+__global__ void __launch_bounds__(256, 2) delta_s(PrepassArgs a) {
+  using T = DsTile<ROWS>;
+  constexpr int KEYS = T::kKeys, CH = T::kCh, NCH = DP / CH;
+  __shared__ __align__(16) float Qs[2][CH][ROWS];
+  __shared__ __align__(16) float Ks[2][CH][KEYS];
+  __shared__ float mu_s[DP];
   const Geometry &g = a.g;
-  const int kt = blockIdx.x, rt = blockIdx.y;
+  const int k0 = blockIdx.x * KEYS, rt = blockIdx.y;
   const int b = blockIdx.z / g.Hkv, hk = blockIdx.z % g.Hkv;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
-  if (!s.ok || kt * kBKV >= s.nkv || s.nq == 0) return;
+  if (!s.ok || k0 >= s.nkv || s.nq == 0) return;
   const int grp = g.Hq / g.Hkv;
   const int nqb = (s.nq + kBQ - 1) / kBQ;
   const int nrows = grp * nqb;
-  const int r0 = rt * kDsRows;
+  const int r0 = rt * ROWS;
   if (r0 >= nrows) return;
-  const int qb_last = min(nrows - 1, r0 + kDsRows - 1) / grp;
-  if (g.causal && kv_tiles_for(qb_last, s.nq, s.nkv, 1) <= kt) return;
+  const int qb_last = min(nrows - 1, r0 + ROWS - 1) / grp;
+  if (g.causal && kv_tiles_for(qb_last, s.nq, s.nkv, 1) <= k0 / kBKV) return;
 
   const int tid = threadIdx.x;
-  const int tr = tid >> 4, tk = tid & 15;
+  const int tr = tid / T::kTk, tk = tid % T::kTk;
+  for (int d = tid; d < DP; d += 256) mu_s[d] = a.w.kmean[((size_t)b * g.Hkv + hk) * DP + d];
+
+  // loader roles. K: vector v = tid + 256 i covers key k0 + v % KEYS, channels
+  // 8 * (v / KEYS) .. + 7 of the chunk. Q means: vector v = tid + 256 i < ROWS * CH / 4 covers
+  // row r0 + v % ROWS, channels 4 * (v / ROWS) .. + 3.
+  const size_t krow_stride = (size_t)g.Hkv * g.D0;
+  uint4 kreg[T::kKVec];
+  float4 qreg[T::kQVec];
+  auto load_chunk = [&](int c0) {
+#pragma unroll
+    for (int i = 0; i < T::kKVec; ++i) {
+      const int v = tid + 256 * i;
+      const int key = k0 + v % KEYS, ch = c0 + 8 * (v / KEYS);
+      kreg[i] = (key < s.nkv && ch < g.D0)
+                    ? __ldg(reinterpret_cast<const uint4 *>(
+                          a.k + (size_t)(s.kv0 + key) * krow_stride + (size_t)hk * g.D0 + ch))
+                    : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < T::kQVec; ++i) {
+      const int v = tid + 256 * i;
+      const int r = r0 + v % ROWS, ch = c0 + 4 * (v / ROWS);
+      qreg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (v < ROWS * (CH / 4) && r < nrows) {
+        const int qb = r / grp, hq = hk * grp + r % grp;
+        qreg[i] = __ldg(reinterpret_cast<const float4 *>(
+            a.w.qmean + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * DP + ch));
+      }
+    }
+  };
+  auto store_chunk = [&](int c0, int buf) {
+#pragma unroll
+    for (int i = 0; i < T::kKVec; ++i) {
+      const int v = tid + 256 * i;
+      const int kl = v % KEYS, cl = 8 * (v / KEYS);
+      float x[8];
+      unpack8<BF16>(kreg[i], x);
+      const bool ok = k0 + kl < s.nkv && c0 + cl < g.D0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        Ks[buf][cl + e][kl] = ok ? __fsub_rn(x[e], mu_s[c0 + cl + e]) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < T::kQVec; ++i) {
+      const int v = tid + 256 * i;
+      if (v < ROWS * (CH / 4)) {
+        const int rl = v % ROWS, cl = 4 * (v / ROWS);
+        Qs[buf][cl][rl] = qreg[i].x;
+        Qs[buf][cl + 1][rl] = qreg[i].y;
+        Qs[buf][cl + 2][rl] = qreg[i].z;
+        Qs[buf][cl + 3][rl] = qreg[i].w;
+      }
+    }
+  };
+
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  // loader roles: row / key = tid / 2, channel half = (tid & 1) * 16 of the 32-channel chunk
-  const int lr = tid >> 1, lh = (tid & 1) * 16;
-  const int key = kt * kBKV + lr;
-  const bool key_ok = key < s.nkv;
-  const uint16_t *ksrc = a.k + (size_t)(s.kv0 + (key_ok ? key : 0)) * g.Hkv * g.D0 + (size_t)hk * g.D0;
-  const float *mu = a.w.kmean + ((size_t)b * g.Hkv + hk) * DP;
-  const int r = r0 + lr;
-  const bool row_ok = r < nrows;
-  const float *qsrc = nullptr;
-  if (row_ok) {
-    const int qb = r / grp, hq = hk * grp + r % grp;
-    qsrc = a.w.qmean + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * DP;
+  // A warp whose rows all lie past the end, or (causal) none of whose rows visits this CTA's
+  // first key tile, skips the FMAs: none of its outputs is written. Warp-uniform.
+  bool warp_busy;
+  {
+    const int w_tr_max = (32 * (tid / 32) + 31) / T::kTk;
+    const int w_row_min = r0 + (32 * (tid / 32)) / T::kTk * 8, w_row_max = r0 + w_tr_max * 8 + 7;
+    warp_busy = w_row_min < nrows;
+    if (warp_busy && g.causal)
+      warp_busy = kv_tiles_for(min(w_row_max, nrows - 1) / grp, s.nq, s.nkv, 1) > k0 / kBKV;
   }
 
+  load_chunk(0);
+  __syncthreads();  // mu_s
+  store_chunk(0, 0);
+  if (NCH > 1) load_chunk(CH);
+  __syncthreads();
 #pragma unroll 1
-  for (int c0 = 0; c0 < DP; c0 += kDsChan) {
-    const int cb = c0 + lh;  // first channel this thread loads
-    float kv[16], qv[16];
-    if (key_ok && cb < g.D0) {
-      float x[8];
-      unpack8(__ldg(reinterpret_cast<const uint4 *>(ksrc + cb)), a.bf16, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) kv[e] = __fsub_rn(x[e], mu[cb + e]);
-      unpack8(__ldg(reinterpret_cast<const uint4 *>(ksrc + cb + 8)), a.bf16, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) kv[8 + e] = __fsub_rn(x[e], mu[cb + 8 + e]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) kv[e] = 0.f;
+  for (int ci = 0; ci < NCH; ++ci) {
+    const int buf = ci & 1;
+    if (ci + 1 < NCH) {  // the other buffer was last read before the previous barrier
+      store_chunk((ci + 1) * CH, buf ^ 1);
+      if (ci + 2 < NCH) load_chunk((ci + 2) * CH);  // in flight during the FMAs below
     }
-    if (row_ok) {
+    if (warp_busy) {
 #pragma unroll
-      for (int e = 0; e < 16; e += 4) {
-        const float4 m4 = __ldg(reinterpret_cast<const float4 *>(qsrc + cb + e));
-        qv[e] = m4.x;
-        qv[e + 1] = m4.y;
-        qv[e + 2] = m4.z;
-        qv[e + 3] = m4.w;
+      for (int d = 0; d < CH; ++d) {
+        const float4 qa = *reinterpret_cast<const float4 *>(&Qs[buf][d][tr * 8]);
+        const float4 qc = *reinterpret_cast<const float4 *>(&Qs[buf][d][tr * 8 + 4]);
+        const float4 ka = *reinterpret_cast<const float4 *>(&Ks[buf][d][tk * 4]);
+        const float4 kc = *reinterpret_cast<const float4 *>(&Ks[buf][d][KEYS / 2 + tk * 4]);
+        const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
+        const float kk[8] = {ka.x, ka.y, ka.z, ka.w, kc.x, kc.y, kc.z, kc.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; j += 2)  // packed: two independent, correctly rounded FMAs
+            fma2(acc[i][j], acc[i][j + 1], qq[i], qq[i], kk[j], kk[j + 1], acc[i][j], acc[i][j + 1]);
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) qv[e] = 0.f;
     }
-    __syncthreads();  // the previous chunk's reads are done
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      Ks[lh + e][lr] = kv[e];
-      Qs[lh + e][lr] = qv[e];
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int d = 0; d < kDsChan; ++d) {
-      const float4 qa = *reinterpret_cast<const float4 *>(&Qs[d][tr * 8]);
-      const float4 qc = *reinterpret_cast<const float4 *>(&Qs[d][tr * 8 + 4]);
-      const float4 ka = *reinterpret_cast<const float4 *>(&Ks[d][tk * 8]);
-      const float4 kc = *reinterpret_cast<const float4 *>(&Ks[d][tk * 8 + 4]);
-      const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
-      const float kk[8] = {ka.x, ka.y, ka.z, ka.w, kc.x, kc.y, kc.z, kc.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; j += 2)  // packed: two independent, correctly rounded FMAs
-          fma2(acc[i][j], acc[i][j + 1], qq[i], qq[i], kk[j], kk[j + 1], acc[i][j], acc[i][j + 1]);
-    }
+    __syncthreads();  // chunk ci + 1 is staged; chunk ci's buffer is free
   }
 
+  const int ntile_kv = (s.nkv + kBKV - 1) / kBKV;  // written tiles stay inside the row stride
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int rr = r0 + tr * 8 + i;
     if (rr >= nrows) break;
     const int qb = rr / grp, hq = hk * grp + rr % grp;
-    if (g.causal && kv_tiles_for(qb, s.nq, s.nkv, 1) <= kt) continue;
-    float *dst = a.w.dsc + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * a.L.nkv_pad +
-                 (size_t)kt * kBKV + tk * 8;
-    float4 lo, hi;
-    lo.x = __fmul_rn(acc[i][0], g.c32);
-    lo.y = __fmul_rn(acc[i][1], g.c32);
-    lo.z = __fmul_rn(acc[i][2], g.c32);
-    lo.w = __fmul_rn(acc[i][3], g.c32);
-    hi.x = __fmul_rn(acc[i][4], g.c32);
-    hi.y = __fmul_rn(acc[i][5], g.c32);
-    hi.z = __fmul_rn(acc[i][6], g.c32);
-    hi.w = __fmul_rn(acc[i][7], g.c32);
-    reinterpret_cast<float4 *>(dst)[0] = lo;
-    reinterpret_cast<float4 *>(dst)[1] = hi;
+    const int vis = g.causal ? kv_tiles_for(qb, s.nq, s.nkv, 1) : ntile_kv;
+    float *row = a.w.dsc + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * a.L.nkv_pad;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int key = k0 + half * (KEYS / 2) + tk * 4;  // 4 keys, one 128-key tile
+      if (key / kBKV >= vis) continue;
+      float4 o;
+      o.x = __fmul_rn(acc[i][4 * half + 0], g.c32);
+      o.y = __fmul_rn(acc[i][4 * half + 1], g.c32);
+      o.z = __fmul_rn(acc[i][4 * half + 2], g.c32);
+      o.w = __fmul_rn(acc[i][4 * half + 3], g.c32);
+      *reinterpret_cast<float4 *>(row + key) = o;
+    }
   }
 }
 
@@ -520,7 +630,7 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   a.q = static_cast<const uint16_t *>(q);
   a.k = static_cast<const uint16_t *>(k);
   a.v = static_cast<const uint16_t *>(v);
-  a.bf16 = in_dtype == SAGE2_BF16;
+  const bool bf16 = in_dtype == SAGE2_BF16;
   a.flags = quant_flags;
   a.g = g;
   a.L = L;
@@ -529,27 +639,45 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   if (e != cudaSuccess) return e;
 
   const int nvec = g.Hkv * g.D0 / 8;
-  int threads = ((nvec + 31) / 32) * 32;
-  threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
-  kv_stats_partial<<<dim3(L.nchunk, g.B), threads, 0, st>>>(a);
-  kv_stats_final<<<g.B * g.Hkv, g.Dp, 0, st>>>(a);
   // every grid dimension at least 1 (a zero-length maximum is legal; the kernels bound-check)
   const int kv_tiles = max(1, (g.max_nkv + kBKV - 1) / kBKV);
   const int q_tiles = max(1, (g.max_nq + kBQ - 1) / kBQ);
+  const dim3 stat_grid(L.nchunk, g.B, (nvec + kStatThreads - 1) / kStatThreads);
   const dim3 kv_grid(kv_tiles, g.Hkv, g.B);
   const dim3 q_grid(q_tiles, g.Hq, g.B);
+  // DeltaS row-tile height: the fewest computed rows for the (Q block, head) rows of a kv
+  // head, the taller tile on ties (more reuse of each staged key)
   const int max_rows = (g.Hq / g.Hkv) * q_tiles;
-  const dim3 ds_grid(kv_tiles, (max_rows + kDsRows - 1) / kDsRows, g.B * g.Hkv);
+  int ds_rows = 128;
+  for (int r : {64, 32})
+    if ((max_rows + r - 1) / r * r < (max_rows + ds_rows - 1) / ds_rows * ds_rows) ds_rows = r;
+  const int ds_keys = kBQ * kBKV / ds_rows;
+  const dim3 ds_grid((max(1, g.max_nkv) + ds_keys - 1) / ds_keys,
+                     (max_rows + ds_rows - 1) / ds_rows, g.B * g.Hkv);
+  // kernels instantiated per padded head dim and input type
+  auto run = [&](auto dp_tag, auto bf_tag) {
+    constexpr int DP = decltype(dp_tag)::value;
+    constexpr bool BF = decltype(bf_tag)::value;
+    kv_stats_partial<BF><<<stat_grid, kStatThreads, 0, st>>>(a);
+    kv_stats_final<<<dim3(g.B * g.Hkv, g.Dp / kFinalChan), kFinalThreads, 0, st>>>(a);
+    k_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
+    v_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
+    q_quant<DP, BF><<<q_grid, 256, 0, st>>>(a);
+    if (ds_rows == 128)
+      delta_s<DP, 128, BF><<<ds_grid, 256, 0, st>>>(a);
+    else if (ds_rows == 64)
+      delta_s<DP, 64, BF><<<ds_grid, 256, 0, st>>>(a);
+    else
+      delta_s<DP, 32, BF><<<ds_grid, 256, 0, st>>>(a);
+  };
+  using T128 = std::integral_constant<int, 128>;
+  using T64 = std::integral_constant<int, 64>;
   if (g.Dp == 128) {
-    k_quant<128><<<kv_grid, 128, 0, st>>>(a);
-    v_quant<128><<<kv_grid, 256, 0, st>>>(a);
-    q_quant<128><<<q_grid, 256, 0, st>>>(a);
-    delta_s<128><<<ds_grid, 256, 0, st>>>(a);
+    if (bf16) run(T128(), std::true_type());
+    else run(T128(), std::false_type());
   } else {
-    k_quant<64><<<kv_grid, 128, 0, st>>>(a);
-    v_quant<64><<<kv_grid, 256, 0, st>>>(a);
-    q_quant<64><<<q_grid, 256, 0, st>>>(a);
-    delta_s<64><<<ds_grid, 256, 0, st>>>(a);
+    if (bf16) run(T64(), std::true_type());
+    else run(T64(), std::false_type());
   }
   return cudaGetLastError();
 }
