@@ -66,12 +66,12 @@ def _load():
         lib.oracle_num_threads.restype = i
         lib.oracle_attention_exact.argtypes = [P, P, P, i, i, P, P, i, i, i, i, f, i, P, i, P]
         lib.oracle_kv_stats.argtypes = [P, P, i, i, P, i, i, i, P, P]
-        lib.oracle_quant_q.argtypes = [P, i, i, P, i, i, i, i, i, i, P, P, P]
-        lib.oracle_quant_k.argtypes = [P, i, i, P, i, i, i, i, P, P, P]
+        lib.oracle_quant_q.argtypes = [P, i, i, P, i, i, i, i, i, i, i, P, P, P]
+        lib.oracle_quant_k.argtypes = [P, i, i, P, i, i, i, i, P, i, P, P]
         lib.oracle_quant_v.argtypes = [P, i, i, P, i, i, i, P, P, P]
         lib.oracle_delta_s.argtypes = [P, i, P, i, i, i, i, i, P, P, P]
         lib.oracle_attention_emulated.argtypes = [P, P, P, i, i, P, P, i, i, i, i, i, f, i, i, i,
-                                                  i, i, i, i, P, i, P, i, P]
+                                                  i, i, i, i, i, P, i, P, i, P]
         _lib = lib
         return lib
 
@@ -167,7 +167,13 @@ def kv_stats(k, v, dtype, cu_kv, Hkv, D0):
     return kmean, vamax
 
 
-def quant_q(q, dtype, cu_q, Hq, D0, bq=128, smooth_q=True, per_block=False):
+def _qmax(qk_bits: int) -> int:
+    if qk_bits not in (4, 8):
+        raise ValueError("qk_bits is 4 (the INT4 grid) or 8 (the INT8 grid)")
+    return (1 << (qk_bits - 1)) - 1
+
+
+def quant_q(q, dtype, cu_q, Hq, D0, bq=128, smooth_q=True, per_block=False, qk_bits=4):
     q = _u16(q)
     cq = _cu(cu_q)
     B, Dp = len(cq) - 1, padded_dim(D0)
@@ -176,18 +182,20 @@ def quant_q(q, dtype, cu_q, Hq, D0, bq=128, smooth_q=True, per_block=False):
     codes = np.zeros((int(cq[-1]), Hq, Dp), np.int8)
     sq = np.zeros((int(cq[-1]), Hq), np.float32)
     _load().oracle_quant_q(_ptr(q), dtype, B, _ptr(cq), Hq, D0, Dp, bq, int(bool(smooth_q)),
-                           int(bool(per_block)), _ptr(qmean), _ptr(codes), _ptr(sq))
+                           int(bool(per_block)), _qmax(qk_bits), _ptr(qmean), _ptr(codes),
+                           _ptr(sq))
     return qmean, codes, sq
 
 
-def quant_k(k, dtype, cu_kv, Hkv, D0, kmean=None, gk=32):
+def quant_k(k, dtype, cu_kv, Hkv, D0, kmean=None, gk=32, qk_bits=4):
     k = _u16(k)
     ck = _cu(cu_kv)
     B, Dp = len(ck) - 1, padded_dim(D0)
     codes = np.zeros((int(ck[-1]), Hkv, Dp), np.int8)
     sk = np.zeros((int(ck[-1]), Hkv), np.float32)
     km = None if kmean is None else np.ascontiguousarray(kmean, dtype=np.float32)
-    _load().oracle_quant_k(_ptr(k), dtype, B, _ptr(ck), Hkv, D0, Dp, gk, _ptr(km), _ptr(codes), _ptr(sk))
+    _load().oracle_quant_k(_ptr(k), dtype, B, _ptr(ck), Hkv, D0, Dp, gk, _ptr(km), _qmax(qk_bits),
+                           _ptr(codes), _ptr(sk))
     return codes, sk
 
 
@@ -219,13 +227,15 @@ def delta_s(k, dtype, cu_kv, b, Hkv, hk, D0, kmean, qbar):
 # ---------------------------------------------------------------- Mode Q
 def attention_emulated(q, k, v, dtype, cu_q, cu_kv, Hq, Hkv, D0, causal, sm_scale=0.0,
                        units=None, bq=128, bkv=128, gk=32, smooth_q=True, smooth_k=True,
-                       per_block=False, acc_bits=0, out=None) -> np.ndarray:
+                       per_block=False, acc_bits=0, qk_bits=4, out=None) -> np.ndarray:
     """The full quantized pipeline (FP64 result before output rounding).
 
     Ablations (the defaults are the method): ``smooth_q`` / ``smooth_k`` off skip the Q block
     mean / K channel mean; ``per_block`` gives Q one scale per block of ``bq`` rows and K one
     per block of ``bkv`` keys instead of the per-thread scales; ``acc_bits > 0`` swaps the
-    two-level P~V fold for one-level accumulation in an ``acc_bits``-bit significand."""
+    two-level P~V fold for one-level accumulation in an ``acc_bits``-bit significand;
+    ``qk_bits=8`` puts the Q and K codes on the INT8 grid [-127, 127] (with ``smooth_q=False,
+    per_block=True``: the SageAttention (v1) path, see ``SAGE1``)."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     cq, ck = _cu(cu_q), _cu(cu_kv)
     B = len(cq) - 1
@@ -235,14 +245,19 @@ def attention_emulated(q, k, v, dtype, cu_q, cu_kv, Hq, Hkv, D0, causal, sm_scal
     _load().oracle_attention_emulated(
         _ptr(q), _ptr(k), _ptr(v), dtype, B, _ptr(cq), _ptr(ck), Hq, Hkv, D0, padded_dim(D0),
         int(bool(causal)), float(sm_scale), bq, bkv, bkv if per_block else gk,
-        int(bool(smooth_q)), int(bool(smooth_k)), int(bool(per_block)), int(acc_bits), _ptr(u), nu,
-        _ptr(out), 0, None)
+        int(bool(smooth_q)), int(bool(smooth_k)), int(bool(per_block)), _qmax(qk_bits),
+        int(acc_bits), _ptr(u), nu, _ptr(out), 0, None)
     return out
+
+
+# The SageAttention (v1) path as a set of switches of the same emulation: INT8 per-block Q and
+# K codes, K smoothed, Q not smoothed (so no Delta-S), P~ and V as in the method.
+SAGE1 = dict(qk_bits=8, per_block=True, smooth_q=False)
 
 
 def emulated_tile_p448(q, k, v, dtype, cu_q, cu_kv, Hq, Hkv, D0, causal, b, h, qb, kt,
                        sm_scale=0.0, bq=128, bkv=128, gk=32, smooth_q=True, smooth_k=True,
-                       per_block=False) -> np.ndarray:
+                       per_block=False, qk_bits=4) -> np.ndarray:
     """The fl32 P448 = 448 * 2^(S' - m_new) of KV tile kt of unit (b, h, qb), as the Mode-Q
     emulation computes it on the way to its output: [bq][bkv], 0 where a key is not visible
     (rows past the sequence end stay 0). The e4m3 code of P~ is oracle.e4m3_encode of it."""
@@ -255,6 +270,6 @@ def emulated_tile_p448(q, k, v, dtype, cu_q, cu_kv, Hq, Hkv, D0, causal, b, h, q
     _load().oracle_attention_emulated(
         _ptr(q), _ptr(k), _ptr(v), dtype, B, _ptr(cq), _ptr(ck), Hq, Hkv, D0, padded_dim(D0),
         int(bool(causal)), float(sm_scale), bq, bkv, bkv if per_block else gk,
-        int(bool(smooth_q)), int(bool(smooth_k)), int(bool(per_block)), 0, _ptr(u), nu,
-        _ptr(out), int(kt), _ptr(dump))
+        int(bool(smooth_q)), int(bool(smooth_k)), int(bool(per_block)), _qmax(qk_bits), 0,
+        _ptr(u), nu, _ptr(out), int(kt), _ptr(dump))
     return dump

@@ -305,14 +305,18 @@ void oracle_kv_stats(const uint16_t *k, const uint16_t *v, int dtype, int B, con
 }
 
 /* ------------------------------------------------------------------------ */
-/* INT4-grid quantizer [R]                                                   */
+/* Symmetric integer-grid quantizer [R]                                      */
 /* ------------------------------------------------------------------------ */
-/* One group of n FP32 values (already smoothed), stride-addressed:
+/* One group of n FP32 values (already smoothed), stride-addressed, onto the
+ * grid [-G, G] (G = qmax):
  *   a = max |x|;  a == 0 -> codes 0, scale 0;
- *   inv = fl32(7 / a);  code = clamp(round_half_even(fl32(x * inv)), -7, 7);
- *   scale = fl32(a / 7).
- * Codes lie on the symmetric INT4 grid [-7, 7] ([P3] component 2). */
-static void quant_group(const float *x, const size_t *idx, int n, int8_t *codes, float *scale) {
+ *   inv = fl32(G / a);  code = clamp(round_half_even(fl32(x * inv)), -G, G);
+ *   scale = fl32(a / G).
+ * G = 7 is the symmetric INT4 grid of the method ([P3] component 2); G = 127
+ * the INT8 grid of the SageAttention (v1) path the research note contrasts it
+ * with ([P3] opening paragraph). */
+static void quant_group(const float *x, const size_t *idx, int n, int qmax, int8_t *codes,
+                        float *scale) {
   float a = 0.f;
   for (int i = 0; i < n; i++) {
     float t = fabsf(x[idx[i]]);
@@ -323,15 +327,16 @@ static void quant_group(const float *x, const size_t *idx, int n, int8_t *codes,
     *scale = 0.f;
     return;
   }
-  const float inv = 7.0f / a;
+  const float g = (float)qmax;
+  const float inv = g / a;
   for (int i = 0; i < n; i++) {
     float t = x[idx[i]] * inv;
     float r = nearbyintf(t);
-    if (r > 7.f) r = 7.f;
-    if (r < -7.f) r = -7.f;
+    if (r > g) r = g;
+    if (r < -g) r = -g;
     codes[idx[i]] = (int8_t)r;
   }
-  *scale = a / 7.0f;
+  *scale = a / g;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -349,7 +354,7 @@ static void quant_group(const float *x, const size_t *idx, int n, int8_t *codes,
  * per-thread scheme improves on, [P3] component 2; ablation only).
  * qmean [B][Hq][nqb_max][Dp], qcodes [total_q][Hq][Dp], sq [total_q][Hq]. */
 void oracle_quant_q(const uint16_t *q, int dtype, int B, const int *cu_q, int Hq, int D0, int Dp,
-                    int bq, int smooth_q, int q_per_block, float *qmean, int8_t *qcodes,
+                    int bq, int smooth_q, int q_per_block, int qmax, float *qmean, int8_t *qcodes,
                     float *sq) {
   int max_nq = 0;
   for (int b = 0; b < B; b++)
@@ -386,7 +391,7 @@ void oracle_quant_q(const uint16_t *q, int dtype, int B, const int *cu_q, int Hq
         }
         if (q_per_block) {
           float sc;
-          quant_group(xt, idx, nr * Dp, ct, &sc);
+          quant_group(xt, idx, nr * Dp, qmax, ct, &sc);
           for (int r = 0; r < nr; r++) {
             const size_t row = (size_t)(cu_q[b] + r0 + r) * Hq + h;
             memcpy(qcodes + row * Dp, ct + (size_t)r * Dp, Dp);
@@ -395,7 +400,7 @@ void oracle_quant_q(const uint16_t *q, int dtype, int B, const int *cu_q, int Hq
         } else {
           for (int r = 0; r < nr; r++) {
             const size_t row = (size_t)(cu_q[b] + r0 + r) * Hq + h;
-            quant_group(xt, idx + (size_t)r * Dp, Dp, ct, sq + row);
+            quant_group(xt, idx + (size_t)r * Dp, Dp, qmax, ct, sq + row);
             memcpy(qcodes + row * Dp, ct + (size_t)r * Dp, Dp);
           }
         }
@@ -414,7 +419,7 @@ void oracle_quant_q(const uint16_t *q, int dtype, int B, const int *cu_q, int Hq
  * chunk by one constant [R]. kcodes [total_kv][Hkv][Dp]; sk [total_kv][Hkv]
  * holds, for every token, the scale of its group. */
 void oracle_quant_k(const uint16_t *k, int dtype, int B, const int *cu_kv, int Hkv, int D0, int Dp,
-                    int gk, const float *kmean, int8_t *kcodes, float *sk) {
+                    int gk, const float *kmean, int qmax, int8_t *kcodes, float *sk) {
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
   for (int b = 0; b < B; b++)
     for (int h = 0; h < Hkv; h++) {
@@ -432,7 +437,7 @@ void oracle_quant_k(const uint16_t *k, int dtype, int B, const int *cu_kv, int H
             idx[t * Dp + d] = (size_t)t * Dp + d;
           }
         float sc;
-        quant_group(xt, idx, cnt * Dp, ct, &sc);
+        quant_group(xt, idx, cnt * Dp, qmax, ct, &sc);
         for (int t = 0; t < cnt; t++) {
           const size_t row = (size_t)(cu_kv[b] + t0 + t) * Hkv + h;
           memcpy(kcodes + row * Dp, ct + (size_t)t * Dp, Dp);
@@ -518,10 +523,13 @@ void oracle_delta_s(const uint16_t *k, int dtype, const int *cu_kv, int b, int H
  *               partial of the two-level scheme; the FP64 sum is exact)
  *     O[i,d]  = fl32(alpha O[i,d] + R[i,d])         (FP32 fold)
  *   out[i,d] = O[i,d] * sv[d] / l   (FP64; 0 when no key is visible).
- * Flags (ablations; smooth_q = smooth_k = 1, q_per_block = acc_bits = 0 is
- * the method): smooth_q, smooth_k; q_per_block (one Q scale per block, see
- * oracle_quant_q; with gk = bkv K gets one scale per block too); acc_bits > 0
- * replaces the two-level fold by one-level accumulation whose accumulator is
+ * Flags (ablations; smooth_q = smooth_k = 1, q_per_block = acc_bits = 0,
+ * qmax = 7 is the method): smooth_q, smooth_k; q_per_block (one Q scale per
+ * block, see oracle_quant_q; with gk = bkv K gets one scale per block too);
+ * qmax the integer grid of the Q and K codes (127: the INT8 path of the
+ * SageAttention (v1) variant, run with smooth_q = 0 and per-block scales:
+ * INT8 with K smoothing, [P3] opening paragraph and its comparison of the two
+ * versions); acc_bits > 0 replaces the two-level fold by one-level accumulation whose accumulator is
  * rounded to acc_bits significand bits after every 32-key MMA step (an
  * emulation of a reduced-precision FP8 MMA accumulator).
  * out [total_q][Hq][D0] (FP64, rows outside `units` untouched).
@@ -539,9 +547,9 @@ static double round_bits(double x, int bits) {
 void oracle_attention_emulated(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
                                int B, const int *cu_q, const int *cu_kv, int Hq, int Hkv, int D0,
                                int Dp, int causal, float sm_scale, int bq, int bkv, int gk,
-                               int smooth_q, int smooth_k, int q_per_block, int acc_bits,
-                               const int *units, int n_units, double *out, int dump_kt,
-                               float *dump_p448) {
+                               int smooth_q, int smooth_k, int q_per_block, int qmax,
+                               int acc_bits, const int *units, int n_units, double *out,
+                               int dump_kt, float *dump_p448) {
   const int g = Hq / Hkv;
   const float scale32 = sm_scale > 0.f ? sm_scale : (float)(1.0 / sqrt((double)D0));
   const float c32 = (float)(1.4426950408889634074 * (double)scale32);
@@ -565,8 +573,8 @@ void oracle_attention_emulated(const uint16_t *q, const uint16_t *k, const uint1
   double e4m3_val[256]; /* value of every e4m3 byte, from the decoder above */
   for (int c = 0; c < 256; c++) e4m3_val[c] = oracle_e4m3_decode((uint8_t)c);
   oracle_kv_stats(k, v, dtype, B, cu_kv, Hkv, D0, Dp, kmean, vamax);
-  oracle_quant_q(q, dtype, B, cu_q, Hq, D0, Dp, bq, smooth_q, q_per_block, qmean, qc, sq);
-  oracle_quant_k(k, dtype, B, cu_kv, Hkv, D0, Dp, gk, smooth_k ? kmean : NULL, kc, sk);
+  oracle_quant_q(q, dtype, B, cu_q, Hq, D0, Dp, bq, smooth_q, q_per_block, qmax, qmean, qc, sq);
+  oracle_quant_k(k, dtype, B, cu_kv, Hkv, D0, Dp, gk, smooth_k ? kmean : NULL, qmax, kc, sk);
   oracle_quant_v(v, dtype, B, cu_kv, Hkv, D0, Dp, vamax, vc, sv);
 
   long total_units = n_units >= 0 ? n_units : (long)B * Hq * nqb;
@@ -616,7 +624,7 @@ void oracle_attention_emulated(const uint16_t *q, const uint16_t *k, const uint1
           }
           const size_t krow = (size_t)(cu_kv[b] + j) * Hkv + hk;
           const int8_t *kj = kc + krow * Dp;
-          int32_t A = 0; /* exact: |A| <= 49 * 128 */
+          int32_t A = 0; /* exact: |A| <= qmax^2 * 128 <= 127^2 * 128 */
           for (int d = 0; d < Dp; d++) A += (int32_t)qi[d] * (int32_t)kj[d];
           const float mult = sqc * sk[krow];
           const float dsc = dS[j] * c32;

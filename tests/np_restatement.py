@@ -50,23 +50,25 @@ def e4m3_value(x: np.float32) -> float:
     return float(t.to(torch.float64)[0])
 
 
-def quantize_group(x: np.ndarray):
-    """x: float32 array (any shape). Returns (int codes, float32 scale)."""
+def quantize_group(x: np.ndarray, g: int = 7):
+    """x: float32 array (any shape), grid [-g, g]. Returns (int codes, float32 scale)."""
     a = F32(np.max(np.abs(x))) if x.size else F32(0)
     if a == 0:
         return np.zeros(x.shape, dtype=np.int64), F32(0)
-    inv = F32(7.0) / a
+    inv = F32(g) / a
     t = (x * inv).astype(F32)
-    codes = np.clip(np.rint(t), -7, 7).astype(np.int64)
-    return codes, F32(a / F32(7.0))
+    codes = np.clip(np.rint(t), -g, g).astype(np.int64)
+    return codes, F32(a / F32(g))
 
 
 def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=128, gk=32,
-           smooth_q=True, smooth_k=True, per_block=False):
+           smooth_q=True, smooth_k=True, per_block=False, qk_bits=4):
     """q, k, v: float64 arrays [tokens, heads, d0] holding the exact fp16/bf16 values.
     Returns the FP64 output before dtype rounding, [total_q, hq, d0].
     Switches: smooth_q / smooth_k off use a zero mean; per_block quantizes each block of bq
-    query rows, and each block of bkv keys, with one scale."""
+    query rows, and each block of bkv keys, with one scale; qk_bits = 8 uses the grid
+    [-127, 127] for the Q and K codes instead of [-7, 7]."""
+    G = 7 if qk_bits == 4 else 127
     g = hq // hkv
     scale32 = F32(sm_scale) if sm_scale > 0 else F32(1.0 / math.sqrt(d0))
     c32 = F32(1.4426950408889634 * float(scale32))
@@ -86,7 +88,7 @@ def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=
             ksc = np.zeros(nkv, F32)
             kg = bkv if per_block else gk
             for t0 in range(0, nkv, kg):
-                cds, s = quantize_group(Kt[t0:t0 + kg])
+                cds, s = quantize_group(Kt[t0:t0 + kg], G)
                 kcodes[t0:t0 + kg] = cds
                 ksc[t0:t0 + kg] = s
             vamax = np.abs(V).max(axis=0).astype(F32) if nkv else np.zeros(d0, F32)
@@ -100,7 +102,7 @@ def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=
                 qbar = np.array([F32(Q[r0:r0 + bq, c].sum() / len(rows)) for c in range(d0)], F32) \
                     if smooth_q else np.zeros(d0, F32)
                 if per_block:
-                    blk_codes, blk_scale = quantize_group((Q[r0:r0 + bq].astype(F32) - qbar).astype(F32))
+                    blk_codes, blk_scale = quantize_group((Q[r0:r0 + bq].astype(F32) - qbar).astype(F32), G)
                 dS = []
                 for j in range(nkv):
                     acc = F32(0)
@@ -109,7 +111,7 @@ def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=
                     dS.append(acc)
                 for i in rows:
                     qt = (Q[i].astype(F32) - qbar).astype(F32)
-                    qc, qs = (blk_codes[i - r0], blk_scale) if per_block else quantize_group(qt)
+                    qc, qs = (blk_codes[i - r0], blk_scale) if per_block else quantize_group(qt, G)
                     sqc = F32(qs * c32)
                     m = -math.inf
                     lsum = 0.0

@@ -330,7 +330,7 @@ def _sm_scale_for_unit_c():
     return float(s)
 
 
-def _zero_error_inputs(seed, nq=24, nkv=40, d0=64, with_means=True):
+def _zero_error_inputs(seed, nq=24, nkv=40, d0=64, with_means=True, g=7, qmean=True):
     """Inputs on which every quantization step is exact ([R] pin of the pipeline):
     Q~ rows come in adjacent +-pairs (so every Q block of even size has mean exactly
     qbar) and K~ rows in +-pairs (channel mean exactly kmean); both sit on the INT4
@@ -341,12 +341,12 @@ def _zero_error_inputs(seed, nq=24, nkv=40, d0=64, with_means=True):
     qt = np.zeros((nq, d0))
     kt = np.zeros((nkv, d0))
     qt[0::2, :2] = rng.integers(-1, 2, size=(nq // 2, 2))
-    qt[0::2, d0 - 2] = 7
+    qt[0::2, d0 - 2] = g
     qt[1::2] = -qt[0::2]
     half_k = nkv // 2
     kt[:half_k, :2] = rng.integers(-1, 2, size=(half_k, 2))
     kt[:half_k, 2] = 2 * rng.integers(-1, 2, size=half_k)
-    kt[:half_k, d0 - 1] = 7
+    kt[:half_k, d0 - 1] = g
     kt[half_k:] = -kt[:half_k]
     kt = kt[rng.permutation(nkv)]
     qbar = np.zeros(d0)
@@ -354,8 +354,9 @@ def _zero_error_inputs(seed, nq=24, nkv=40, d0=64, with_means=True):
     if with_means:
         # |A| <= 2 and |dS| <= 3; the 0.5 in channel 2 meets even K~ values only, so dS
         # stays an integer, while an unsmoothed Q would round that 0.5 away
-        qbar[:2] = rng.integers(-1, 2, size=2)
-        qbar[2] = 0.5
+        if qmean:
+            qbar[:2] = rng.integers(-1, 2, size=2)
+            qbar[2] = 0.5
         kmean[4:8] = rng.integers(-3, 4, size=4)
     q = qt + qbar
     k = kt + kmean
@@ -383,11 +384,57 @@ def test_zero_rounding_error_reduces_to_exact(oracle_mod, with_means, causal):
         assert not np.allclose(bad, ex, rtol=1e-3)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_int8_path_with_zero_rounding_error_reduces_to_exact(oracle_mod, causal):
+    """The SageAttention (v1) switches (INT8 per-block Q and K codes, K smoothed, Q not):
+    inputs on the INT8 grid with a 127 in every row (every scale 1) and a K channel mean
+    pass through exactly; a quantizer still on the INT4 grid would not."""
+    q, k, v = _zero_error_inputs(7, g=127, qmean=False)
+    T = lambda a: torch.tensor(a)[:, None, :].half()
+    args = (bits(T(q)), bits(T(k)), bits(T(v)), F16, [0, len(q)], [0, len(k)], 1, 1, 64, causal,
+            _sm_scale_for_unit_c())
+    emu = oracle_mod.attention_emulated(*args, bq=8, bkv=16, **oracle_mod.SAGE1)
+    ex = oracle_mod.attention_exact(*args)
+    np.testing.assert_allclose(emu, ex, rtol=2e-6, atol=448 * 1e-7)
+    bad = oracle_mod.attention_emulated(*args, bq=8, bkv=16, per_block=True, smooth_q=False)
+    assert not np.allclose(bad, ex, rtol=1e-3)
+
+
+def test_int8_quantizer_invariants(oracle_mod):
+    """INT8 grid: codes in [-127, 127], 127 reached in every non-zero group, rounding within
+    half a step, scale = amax / 127; per-block Q blocks share one scale."""
+    w = W.scaled(W.PREFILL, (300,), (300,), hq=2, hkv=2)
+    x = W.make_inputs(w)
+    km, _ = oracle_mod.kv_stats(bits(x["k"]), bits(x["v"]), BF16, x["cu_kv"], 2, 128)
+    kc, sk = oracle_mod.quant_k(bits(x["k"]), BF16, x["cu_kv"], 2, 128, kmean=km, gk=128,
+                                qk_bits=8)
+    qm, qc, sq = oracle_mod.quant_q(bits(x["q"]), BF16, x["cu_q"], 2, 128, smooth_q=False,
+                                    per_block=True, qk_bits=8)
+    assert np.all(qm == 0)
+    k64, q64 = x["k"].double().numpy(), x["q"].double().numpy()
+    for h in range(2):
+        kt = (k64[:, h].astype(np.float32) - km[0, h]).astype(np.float32)
+        for t0 in range(0, 300, 128):
+            grp = slice(t0, min(300, t0 + 128))
+            assert len(set(sk[grp, h].tolist())) == 1
+            s = sk[grp, h][0]
+            assert s == np.float32(np.abs(kt[grp]).max() / np.float32(127))
+            c = kc[grp, h]
+            assert c.min() >= -127 and c.max() <= 127 and np.abs(c).max() == 127
+            assert np.abs(kt[grp] - c * float(s)).max() <= 0.5 * float(s) * (1 + 1e-5)
+            qb = q64[grp, h].astype(np.float32)
+            assert len(set(sq[grp, h].tolist())) == 1
+            assert np.abs(qc[grp, h]).max() == 127
+            assert np.abs(qb - qc[grp, h] * float(sq[grp, h][0])).max() <= 0.5 * float(sq[grp, h][0]) * (1 + 1e-5)
+
+
 ABLATION_FLAGS = [dict(), dict(smooth_q=False), dict(smooth_k=False), dict(per_block=True),
-                  dict(smooth_q=False, smooth_k=False, per_block=True)]
+                  dict(smooth_q=False, smooth_k=False, per_block=True),
+                  dict(qk_bits=8, per_block=True, smooth_q=False), dict(qk_bits=8)]
 
 
-@pytest.mark.parametrize("flags", ABLATION_FLAGS, ids=["method", "noQs", "noKs", "block", "naive"])
+@pytest.mark.parametrize("flags", ABLATION_FLAGS,
+                         ids=["method", "noQs", "noKs", "block", "naive", "sage1", "int8thread"])
 @pytest.mark.parametrize("case", [
     dict(nq=(5,), nkv=(7,), hq=2, hkv=1, d0=4, causal=False, dtype="fp16", dist="tiny"),
     dict(nq=(6, 3), nkv=(4, 8), hq=2, hkv=2, d0=8, causal=True, dtype="bf16", dist="outlier"),
@@ -514,6 +561,19 @@ def test_per_thread_granularity_beats_per_block(oracle_mod, outlier_case):
     e_naive = relL1(_emu(oracle_mod, w, x, per_block=True, smooth_q=False, smooth_k=False), ex)
     assert e_block > 1.2 * e_thread
     assert e_naive > e_block
+
+
+def test_int8_path_errs_less_than_int4(oracle_mod, outlier_case):
+    """The INT8 grid is 18 times finer than the INT4 one: the SageAttention (v1) path (INT8
+    per-block, K smoothed) errs less against exact attention than the method's INT4 path,
+    which pays for its 4-bit matrix multiply with the repairs (the pages' trade-off)."""
+    w, x = outlier_case
+    ex = oracle_mod.attention_exact(bits(x["q"]), bits(x["k"]), bits(x["v"]), W.dtype_code(w),
+                                    x["cu_q"], x["cu_kv"], w.hq, w.hkv, w.d, w.causal)
+    e_v2 = relL1(_emu(oracle_mod, w, x), ex)
+    e_v1 = relL1(_emu(oracle_mod, w, x, **oracle_mod.SAGE1), ex)
+    e_v1_int4 = relL1(_emu(oracle_mod, w, x, per_block=True, smooth_q=False), ex)
+    assert e_v1 < e_v2 < e_v1_int4
 
 
 def test_two_level_accumulation_beats_one_level(oracle_mod, outlier_case):
