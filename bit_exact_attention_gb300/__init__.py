@@ -23,12 +23,13 @@ __all__ = ["attn_fwd", "attn_fwd_varlen", "prepass", "attention", "prepass_varle
            "attention_varlen", "workspace_size", "workspace_layout", "device_status",
            "alloc_workspace", "debug_tile", "debug_timeout", "Sage2Error", "load_library",
            "attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "quant_flags", "QUANT_NO_SMOOTH_Q",
-           "QUANT_NO_SMOOTH_K", "QUANT_PER_BLOCK"]
+           "QUANT_NO_SMOOTH_K", "QUANT_PER_BLOCK", "QUANT_SAGE1"]
 
 _DT = {torch.float16: FP16, torch.bfloat16: BF16, torch.float32: FP32}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # SAGE2_NOALLOC_SCRATCH_BYTES in include/sage2_attn.h
-# sage2_quant_flags in include/sage2_attn.h: accuracy ablations; 0 is the method
-QUANT_NO_SMOOTH_Q, QUANT_NO_SMOOTH_K, QUANT_PER_BLOCK = 1, 2, 4
+# sage2_quant_flags in include/sage2_attn.h: accuracy ablations (0 is the method), and the
+# SageAttention (v1) path: INT8 per-block Q and K codes, K smoothed, Q not
+QUANT_NO_SMOOTH_Q, QUANT_NO_SMOOTH_K, QUANT_PER_BLOCK, QUANT_SAGE1 = 1, 2, 4, 8
 
 
 def quant_flags(smooth_q: bool = True, smooth_k: bool = True, per_block: bool = False) -> int:
@@ -65,22 +66,28 @@ def _dev(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
-def workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q=None, total_kv=None) -> int:
+def workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q=None, total_kv=None,
+                   quant_flags=0) -> int:
     total_q = B * max_nq if total_q is None else total_q
     total_kv = B * max_nkv if total_kv is None else total_kv
-    n = _lib.lib().sage2_workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv)
+    if quant_flags:
+        n = _lib.lib().sage2_workspace_size_ex(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv,
+                                               int(quant_flags))
+    else:
+        n = _lib.lib().sage2_workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv)
     if n == 0:
         raise Sage2Error(_lib.EINVAL, "sage2_workspace_size")
     return int(n)
 
 
-def workspace_layout(B, Hq, Hkv, max_nq, max_nkv, D, total_q=None, total_kv=None) -> WsLayout:
+def workspace_layout(B, Hq, Hkv, max_nq, max_nkv, D, total_q=None, total_kv=None,
+                     quant_flags=0) -> WsLayout:
     total_q = B * max_nq if total_q is None else total_q
     total_kv = B * max_nkv if total_kv is None else total_kv
     L = WsLayout()
-    _lib.check(_lib.lib().sage2_workspace_layout(B, Hq, Hkv, max_nq, max_nkv, D, total_q,
-                                                 total_kv, ctypes.byref(L)),
-               "sage2_workspace_layout")
+    _lib.check(_lib.lib().sage2_workspace_layout_ex(B, Hq, Hkv, max_nq, max_nkv, D, total_q,
+                                                    total_kv, int(quant_flags), ctypes.byref(L)),
+               "sage2_workspace_layout_ex")
     return L
 
 
@@ -157,12 +164,13 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, causa
     B = cu_seqlens_q.numel() - 1
     odt = q.dtype if out_dtype is None else out_dtype
     out = _out(out, (total_q, Hq, D), odt, q.device)
-    ws = _ws(workspace, workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv), q.device)
+    ws = _ws(workspace, workspace_size(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv,
+                                       quant_flags), q.device)
     if quant_flags:
         prepass_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, ws, causal=causal,
                        sm_scale=sm_scale, stream=stream, quant_flags=quant_flags)
         attention_varlen(out, ws, cu_seqlens_q, cu_seqlens_kv, Hkv, max_nq, max_nkv, total_kv,
-                         causal=causal, sm_scale=sm_scale, stream=stream)
+                         causal=causal, sm_scale=sm_scale, stream=stream, quant_flags=quant_flags)
         return out
     _lib.check(_lib.lib().sage2_attn_fwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _code(q.dtype), _code(out.dtype),
@@ -205,9 +213,16 @@ def prepass_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_nq, max_nkv, worksp
 
 
 def attention_varlen(out, workspace, cu_seqlens_q, cu_seqlens_kv, Hkv, max_nq, max_nkv,
-                     total_kv, causal=False, sm_scale=0.0, stream=None):
+                     total_kv, causal=False, sm_scale=0.0, stream=None, quant_flags=0):
     total_q, Hq, D = out.shape
     B = cu_seqlens_q.numel() - 1
+    if quant_flags:
+        _lib.check(_lib.lib().sage2_attention_varlen_ex(
+            _ptr(out), _code(out.dtype), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq, Hkv,
+            max_nq, max_nkv, total_q, total_kv, D, int(bool(causal)), float(sm_scale),
+            int(quant_flags), _ptr(workspace), workspace.numel(), _stream(stream)),
+            "sage2_attention_varlen_ex")
+        return
     _lib.check(_lib.lib().sage2_attention_varlen(
         _ptr(out), _code(out.dtype), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq, Hkv, max_nq,
         max_nkv, total_q, total_kv, D, int(bool(causal)), float(sm_scale), _ptr(workspace),
@@ -222,7 +237,8 @@ def device_status(workspace, stream=None) -> tuple[int, int]:
 
 
 def debug_tile(workspace, B, Hq, Hkv, max_nq, max_nkv, D, causal, b, h, qt, kt, sm_scale=0.0,
-               cu_seqlens_q=None, cu_seqlens_kv=None, total_q=None, total_kv=None, stream=None):
+               cu_seqlens_q=None, cu_seqlens_kv=None, total_q=None, total_kv=None, stream=None,
+               quant_flags=0):
     """Raw (S accumulators, P~ bytes, fresh P~V partial) of one KV tile of one work unit."""
     dev = workspace.device
     Dp = 64 if D <= 64 else 128
@@ -231,10 +247,11 @@ def debug_tile(workspace, B, Hq, Hkv, max_nq, max_nkv, D, causal, b, h, qt, kt, 
     r_out = torch.zeros(128, Dp, dtype=torch.float32, device=dev)
     total_q = B * max_nq if total_q is None else total_q
     total_kv = B * max_nkv if total_kv is None else total_kv
-    _lib.check(_lib.lib().sage2_debug_tile(
+    _lib.check(_lib.lib().sage2_debug_tile_ex(
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Hq, Hkv, max_nq, max_nkv, total_q, total_kv,
-        D, int(bool(causal)), float(sm_scale), _ptr(workspace), workspace.numel(), b, h, qt, kt,
-        _ptr(s_out), _ptr(p_out), _ptr(r_out), _stream(stream)), "sage2_debug_tile")
+        D, int(bool(causal)), float(sm_scale), int(quant_flags), _ptr(workspace),
+        workspace.numel(), b, h, qt, kt, _ptr(s_out), _ptr(p_out), _ptr(r_out), _stream(stream)),
+        "sage2_debug_tile_ex")
     return s_out, p_out, r_out
 
 

@@ -30,7 +30,7 @@ class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "total_bytes", "qcode", "kcode", "vcodeT", "qscale", "kscale", "qmean", "kmean", "vscale",
         "vinv", "dsc", "kpart", "vpart", "status")] + [
-        (n, ctypes.c_int) for n in ("Dp", "Tq", "Tkv", "nkv_pad", "nchunk")]
+        (n, ctypes.c_int) for n in ("Dp", "Tq", "Tkv", "nkv_pad", "nchunk", "code_bytes")]
 
 
 def header_functions() -> list[str]:
@@ -48,6 +48,8 @@ def _declare(lib):
         "sage2_version": ([], i),
         "sage2_workspace_size": ([i] * 8, sz),
         "sage2_workspace_layout": ([i] * 8 + [ctypes.POINTER(WsLayout)], i),
+        "sage2_workspace_size_ex": ([i] * 9, sz),
+        "sage2_workspace_layout_ex": ([i] * 9 + [ctypes.POINTER(WsLayout)], i),
         "sage2_attn_fwd": ([P, P, P, P, i, i, i, i, i, i, i, i, i, f, P, sz, P], i),
         "sage2_attn_fwd_varlen": ([P, P, P, P, i, i, P, P, i, i, i, i, i, i, i, i, i, f, P, sz, P], i),
         "sage2_prepass": ([P, P, P, i, i, i, i, i, i, i, i, f, P, sz, P], i),
@@ -55,8 +57,11 @@ def _declare(lib):
         "sage2_prepass_varlen": ([P, P, P, i, P, P, i, i, i, i, i, i, i, i, i, f, P, sz, P], i),
         "sage2_prepass_varlen_ex": ([P, P, P, i, P, P, i, i, i, i, i, i, i, i, i, f, i, P, sz, P], i),
         "sage2_attention_varlen": ([P, i, P, P, i, i, i, i, i, i, i, i, i, f, P, sz, P], i),
+        "sage2_attention_varlen_ex": ([P, i, P, P, i, i, i, i, i, i, i, i, i, f, i, P, sz, P], i),
         "sage2_device_status": ([P, P, ctypes.POINTER(i)], i),
         "sage2_debug_tile": ([P, P, i, i, i, i, i, i, i, i, i, f, P, sz, i, i, i, i, P, P, P, P], i),
+        "sage2_debug_tile_ex": ([P, P, i, i, i, i, i, i, i, i, i, f, i, P, sz, i, i, i, i, P, P, P, P],
+                                i),
         "sage2_debug_timeout": ([i, i, i, i, i, i, P, sz, P], i),
         "sage2_attn_fwd_noalloc": ([P, P, P, P, i, i, i, i, i, i, i, i, i, f, P], i),
     }

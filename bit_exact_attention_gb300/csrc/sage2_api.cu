@@ -12,7 +12,8 @@ namespace sage2 {
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool make_layout(int B, int Hq, int Hkv, int max_nq, int max_nkv, int Dp, int total_q,
-                 int total_kv, Layout *L) {
+                 int total_kv, int code_bytes, Layout *L) {
+  if (code_bytes != 1 && code_bytes != 2) return false;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || max_nq < 0 || max_nkv < 0 || total_q < 0 || total_kv < 0)
     return false;
   // padded rows: every sequence starts at 128 * (cu[b] / 128 + b) and occupies a whole
@@ -35,9 +36,10 @@ bool make_layout(int B, int Hq, int Hkv, int max_nq, int max_nkv, int Dp, int to
     off = align_up(off + bytes, 1024);
     return o;
   };
+  L->code_bytes = code_bytes;
   L->status = take(256);
-  L->qcode = take((size_t)Hq * tq * Dp);
-  L->kcode = take((size_t)Hkv * tkv * Dp);
+  L->qcode = take((size_t)Hq * tq * Dp * code_bytes);
+  L->kcode = take((size_t)Hkv * tkv * Dp * code_bytes);
   L->vcodeT = take((size_t)Hkv * Dp * tkv);
   L->qscale = take((size_t)Hq * tq * 4);
   L->kscale = take((size_t)Hkv * (tkv / kGK) * 4);
@@ -112,7 +114,7 @@ static int check_shapes(int B, int Hq, int Hkv, int max_nq, int max_nkv, int D, 
 
 static bool make_geometry(int B, int Hq, int Hkv, int max_nq, int max_nkv, int D, int total_q,
                           int total_kv, int causal, float sm_scale, const int *cu_q,
-                          const int *cu_kv, Geometry *g, Layout *L) {
+                          const int *cu_kv, int code_bytes, Geometry *g, Layout *L) {
   g->B = B;
   g->Hq = Hq;
   g->Hkv = Hkv;
@@ -127,8 +129,16 @@ static bool make_geometry(int B, int Hq, int Hkv, int max_nq, int max_nkv, int D
   g->cu_kv = cu_kv;
   g->sm_scale = sm_scale > 0.f ? sm_scale : (float)(1.0 / sqrt((double)D));
   g->c32 = (float)(1.4426950408889634074 * (double)g->sm_scale);
-  return make_layout(B, Hq, Hkv, max_nq, max_nkv, g->Dp, total_q, total_kv, L);
+  return make_layout(B, Hq, Hkv, max_nq, max_nkv, g->Dp, total_q, total_kv, code_bytes, L);
 }
+
+// Quantization switches: the ablation bits in any combination, or SAGE2_QUANT_SAGE1 alone.
+static bool valid_quant_flags(int f) {
+  const int ablations = SAGE2_QUANT_NO_SMOOTH_Q | SAGE2_QUANT_NO_SMOOTH_K | SAGE2_QUANT_PER_BLOCK;
+  if (f & SAGE2_QUANT_SAGE1) return f == SAGE2_QUANT_SAGE1;
+  return (f & ~ablations) == 0;
+}
+static int code_bytes_of(int quant_flags) { return (quant_flags & SAGE2_QUANT_SAGE1) ? 2 : 1; }
 
 static int check_ws(const void *ws, size_t bytes, const Layout &L) {
   if (!ws || !aligned16(ws)) return SAGE2_EWORKSPACE;
@@ -147,15 +157,14 @@ static int prepass_impl(const void *q, const void *k, const void *v, int in_dtyp
   int rc = check_shapes(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
   if (in_dtype != SAGE2_FP16 && in_dtype != SAGE2_BF16) return SAGE2_EINVAL;
-  if (quant_flags & ~(SAGE2_QUANT_NO_SMOOTH_Q | SAGE2_QUANT_NO_SMOOTH_K | SAGE2_QUANT_PER_BLOCK))
-    return SAGE2_EINVAL;
+  if (!valid_quant_flags(quant_flags)) return SAGE2_EINVAL;
   if ((total_q > 0 && (!q || !aligned16(q))) || (total_kv > 0 && (!k || !v || !aligned16(k) ||
                                                                   !aligned16(v))))
     return SAGE2_EINVAL;
   Geometry g;
   Layout L;
   if (!make_geometry(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal, sm_scale, cu_q,
-                     cu_kv, &g, &L))
+                     cu_kv, code_bytes_of(quant_flags), &g, &L))
     return SAGE2_EINVAL;
   if ((rc = check_ws(ws, ws_bytes, L))) return rc;
   if ((rc = check_device())) return rc;
@@ -163,25 +172,26 @@ static int prepass_impl(const void *q, const void *k, const void *v, int in_dtyp
       launch_prepass(q, k, v, in_dtype, quant_flags, g, L, ws, (cudaStream_t)stream));
 }
 
-static int attention_impl(void *out, int out_dtype, int in_dtype_hint, const int *cu_q,
+static int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q,
                           const int *cu_kv, int B, int Hq, int Hkv, int max_nq, int max_nkv,
                           int total_q, int total_kv, int D, int causal, float sm_scale,
                           const void *ws, size_t ws_bytes, void *stream) {
-  (void)in_dtype_hint;
   int rc = check_shapes(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
+  if (!valid_quant_flags(quant_flags)) return SAGE2_EINVAL;
   if (out_dtype != SAGE2_FP16 && out_dtype != SAGE2_BF16 && out_dtype != SAGE2_FP32)
     return SAGE2_EINVAL;
   if (total_q > 0 && (!out || !aligned16(out))) return SAGE2_EINVAL;
   Geometry g;
   Layout L;
   if (!make_geometry(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal, sm_scale, cu_q,
-                     cu_kv, &g, &L))
+                     cu_kv, code_bytes_of(quant_flags), &g, &L))
     return SAGE2_EINVAL;
   if ((rc = check_ws(ws, ws_bytes, L))) return rc;
   if ((rc = check_device())) return rc;
   if (total_q == 0 || max_nq == 0) return SAGE2_OK;
-  return cuda_status(launch_attention(out, out_dtype, g, L, ws, (cudaStream_t)stream, nullptr));
+  return cuda_status(launch_attention(out, out_dtype, g, L, ws, (cudaStream_t)stream, nullptr,
+                                      (quant_flags & SAGE2_QUANT_SAGE1) != 0));
 }
 
 }  // namespace sage2
@@ -204,21 +214,35 @@ const char *sage2_status_str(int s) {
 
 int sage2_version(void) { return 100; }
 
+size_t sage2_workspace_size_ex(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D,
+                               int total_q, int total_kv, int quant_flags) {
+  if (check_shapes(B, Hq, Hkv, max_Nq, max_Nkv, D, total_q, total_kv, 0)) return 0;
+  if (!valid_quant_flags(quant_flags)) return 0;
+  Layout L;
+  if (!make_layout(B, Hq, Hkv, max_Nq, max_Nkv, padded_dim(D), total_q, total_kv,
+                   code_bytes_of(quant_flags), &L))
+    return 0;
+  return L.total;
+}
+
 size_t sage2_workspace_size(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D, int total_q,
                             int total_kv) {
-  if (check_shapes(B, Hq, Hkv, max_Nq, max_Nkv, D, total_q, total_kv, 0)) return 0;
-  Layout L;
-  if (!make_layout(B, Hq, Hkv, max_Nq, max_Nkv, padded_dim(D), total_q, total_kv, &L)) return 0;
-  return L.total;
+  return sage2_workspace_size_ex(B, Hq, Hkv, max_Nq, max_Nkv, D, total_q, total_kv, 0);
 }
 
 int sage2_workspace_layout(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D, int total_q,
                            int total_kv, sage2_ws_layout *out) {
+  return sage2_workspace_layout_ex(B, Hq, Hkv, max_Nq, max_Nkv, D, total_q, total_kv, 0, out);
+}
+
+int sage2_workspace_layout_ex(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D,
+                              int total_q, int total_kv, int quant_flags, sage2_ws_layout *out) {
   int rc = check_shapes(B, Hq, Hkv, max_Nq, max_Nkv, D, total_q, total_kv, 0);
   if (rc) return rc;
-  if (!out) return SAGE2_EINVAL;
+  if (!out || !valid_quant_flags(quant_flags)) return SAGE2_EINVAL;
   Layout L;
-  if (!make_layout(B, Hq, Hkv, max_Nq, max_Nkv, padded_dim(D), total_q, total_kv, &L))
+  if (!make_layout(B, Hq, Hkv, max_Nq, max_Nkv, padded_dim(D), total_q, total_kv,
+                   code_bytes_of(quant_flags), &L))
     return SAGE2_EINVAL;
   out->total_bytes = L.total;
   out->qcode = L.qcode;
@@ -239,6 +263,7 @@ int sage2_workspace_layout(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int 
   out->Tkv = L.Tkv;
   out->nkv_pad = L.nkv_pad;
   out->nchunk = L.nchunk;
+  out->code_bytes = L.code_bytes;
   return SAGE2_OK;
 }
 
@@ -276,7 +301,7 @@ int sage2_attention(void *out, int out_dtype, int B, int Hq, int Hkv, int Nq, in
                     int causal, float sm_scale, const void *workspace, size_t workspace_bytes,
                     void *stream) {
   if ((long long)B * Nq >= (1LL << 31) || (long long)B * Nkv >= (1LL << 31)) return SAGE2_EINVAL;
-  return attention_impl(out, out_dtype, -1, nullptr, nullptr, B, Hq, Hkv, Nq, Nkv, B * Nq,
+  return attention_impl(out, out_dtype, 0, nullptr, nullptr, B, Hq, Hkv, Nq, Nkv, B * Nq,
                         B * Nkv, D, causal, sm_scale, workspace, workspace_bytes, stream);
 }
 
@@ -286,8 +311,19 @@ int sage2_attention_varlen(void *out, int out_dtype, const int *cu_seqlens_q,
                            float sm_scale, const void *workspace, size_t workspace_bytes,
                            void *stream) {
   if (!cu_seqlens_q || !cu_seqlens_kv) return SAGE2_EINVAL;
-  return attention_impl(out, out_dtype, -1, cu_seqlens_q, cu_seqlens_kv, B, Hq, Hkv, max_Nq,
+  return attention_impl(out, out_dtype, 0, cu_seqlens_q, cu_seqlens_kv, B, Hq, Hkv, max_Nq,
                         max_Nkv, total_q, total_kv, D, causal, sm_scale, workspace,
+                        workspace_bytes, stream);
+}
+
+int sage2_attention_varlen_ex(void *out, int out_dtype, const int *cu_seqlens_q,
+                              const int *cu_seqlens_kv, int B, int Hq, int Hkv, int max_Nq,
+                              int max_Nkv, int total_q, int total_kv, int D, int causal,
+                              float sm_scale, int quant_flags, const void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  if (!cu_seqlens_q || !cu_seqlens_kv) return SAGE2_EINVAL;
+  return attention_impl(out, out_dtype, quant_flags, cu_seqlens_q, cu_seqlens_kv, B, Hq, Hkv,
+                        max_Nq, max_Nkv, total_q, total_kv, D, causal, sm_scale, workspace,
                         workspace_bytes, stream);
 }
 
@@ -335,7 +371,7 @@ int sage2_device_status(const void *workspace, void *stream, int *raw) {
     return SAGE2_ECUDA;
   if (raw) *raw = word;
   if (word == 0) return SAGE2_OK;
-  if (word == kStatusSeqTooLong) return SAGE2_EINVAL;
+  if (word == kStatusSeqTooLong || word == kStatusFormat) return SAGE2_EINVAL;
   return SAGE2_EDEVICE_TIMEOUT;
 }
 
@@ -343,15 +379,26 @@ int sage2_debug_tile(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, i
                      int max_Nq, int max_Nkv, int total_q, int total_kv, int D, int causal,
                      float sm_scale, const void *workspace, size_t workspace_bytes, int b, int h,
                      int qt, int kt, float *s_out, uint8_t *p_out, float *r_out, void *stream) {
+  return sage2_debug_tile_ex(cu_seqlens_q, cu_seqlens_kv, B, Hq, Hkv, max_Nq, max_Nkv, total_q,
+                             total_kv, D, causal, sm_scale, 0, workspace, workspace_bytes, b, h,
+                             qt, kt, s_out, p_out, r_out, stream);
+}
+
+int sage2_debug_tile_ex(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq,
+                        int Hkv, int max_Nq, int max_Nkv, int total_q, int total_kv, int D,
+                        int causal, float sm_scale, int quant_flags, const void *workspace,
+                        size_t workspace_bytes, int b, int h, int qt, int kt, float *s_out,
+                        uint8_t *p_out, float *r_out, void *stream) {
   int rc = check_shapes(B, Hq, Hkv, max_Nq, max_Nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
+  if (!valid_quant_flags(quant_flags)) return SAGE2_EINVAL;
   if ((cu_seqlens_q == nullptr) != (cu_seqlens_kv == nullptr)) return SAGE2_EINVAL;
   if (!s_out || !p_out || !r_out || b < 0 || b >= B || h < 0 || h >= Hq || qt < 0 || kt < 0)
     return SAGE2_EINVAL;
   Geometry g;
   Layout L;
   if (!make_geometry(B, Hq, Hkv, max_Nq, max_Nkv, D, total_q, total_kv, causal, sm_scale,
-                     cu_seqlens_q, cu_seqlens_kv, &g, &L))
+                     cu_seqlens_q, cu_seqlens_kv, code_bytes_of(quant_flags), &g, &L))
     return SAGE2_EINVAL;
   if ((rc = check_ws(workspace, workspace_bytes, L))) return rc;
   if ((rc = check_device())) return rc;
@@ -361,7 +408,8 @@ int sage2_debug_tile(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, i
   const size_t out_bytes = (size_t)(total_q > 0 ? total_q : 1) * Hq * D * sizeof(float);
   if (cudaMallocAsync(&scratch, out_bytes, (cudaStream_t)stream) != cudaSuccess) return SAGE2_ECUDA;
   AttnDebug dbg{b, h, qt, kt, s_out, p_out, r_out, 0};
-  cudaError_t e = launch_attention(scratch, SAGE2_FP32, g, L, workspace, (cudaStream_t)stream, &dbg);
+  cudaError_t e = launch_attention(scratch, SAGE2_FP32, g, L, workspace, (cudaStream_t)stream, &dbg,
+                                   (quant_flags & SAGE2_QUANT_SAGE1) != 0);
   cudaFreeAsync(scratch, (cudaStream_t)stream);
   return cuda_status(e);
 }
@@ -373,7 +421,7 @@ int sage2_debug_timeout(int B, int Hq, int Hkv, int Nq, int Nkv, int D, const vo
   if (Nq <= 0 || Nkv <= 0) return SAGE2_EINVAL;
   Geometry g;
   Layout L;
-  if (!make_geometry(B, Hq, Hkv, Nq, Nkv, D, B * Nq, B * Nkv, 0, 0.f, nullptr, nullptr, &g, &L))
+  if (!make_geometry(B, Hq, Hkv, Nq, Nkv, D, B * Nq, B * Nkv, 0, 0.f, nullptr, nullptr, 1, &g, &L))
     return SAGE2_EINVAL;
   if ((rc = check_ws(workspace, workspace_bytes, L))) return rc;
   if ((rc = check_device())) return rc;

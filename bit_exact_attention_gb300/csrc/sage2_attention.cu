@@ -98,10 +98,13 @@ struct AttnArgs {
   AttnDebug dbg;
 };
 
-template <int DP, int ST>
+template <int DP, int ST, bool I8>
 struct SmemPlan {
+  // K codes: e4m3 bytes, or fp16 values of the INT8-grid codes (I8) stored as DP / 64 blocks of
+  // 64 channels (128-byte swizzled rows, 16 KB per block)
+  static constexpr int kKStage = 128 * DP * (I8 ? 2 : 1);
   static constexpr int kK = 0;                           // [ST][128 keys][DP]     (swizzled)
-  static constexpr int kV = kK + ST * 128 * DP;          // [ST][DP][128 keys]     (swizzled)
+  static constexpr int kV = kK + ST * kKStage;           // [ST][DP][128 keys]     (swizzled)
   static constexpr int kDsc = kV + ST * DP * 128;        // float [ST][128]
   static constexpr int kSk = kDsc + ST * 512;            // float [ST][4]
   static constexpr int kAlpha = kSk + ST * 16;           // float [4][128]
@@ -129,6 +132,8 @@ __device__ __forceinline__ bool warp_all(bool ok) {
 }
 
 // S' = A * (s_q c s_k) + DeltaS c for 64 keys (one FMA each), masked beyond `lim`, and their max.
+// Without DeltaS (the INT8 path, no Q smoothing) the addend is +0, as in the definition.
+template <bool DS>
 __device__ __forceinline__ float logits64(float (&x)[64], const uint32_t (&v)[64], const float *dsc,
                                           const float *skv, float sqc, int lim) {
 #pragma unroll
@@ -136,7 +141,8 @@ __device__ __forceinline__ float logits64(float (&x)[64], const uint32_t (&v)[64
     const float mult = __fmul_rn(sqc, skv[c]);
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
-      const float4 d4 = *reinterpret_cast<const float4 *>(dsc + c * 32 + e);
+      const float4 d4 =
+          DS ? *reinterpret_cast<const float4 *>(dsc + c * 32 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
       const int k0 = c * 32 + e;
       fma2(x[k0], x[k0 + 1], __uint_as_float(v[k0]), __uint_as_float(v[k0 + 1]), mult, mult, d4.x,
            d4.y);
@@ -169,16 +175,21 @@ __device__ __forceinline__ void cta_teardown(bool owner, uint32_t tbase) {
   if (owner) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <int DP, int ST, bool DBG>
+template <int DP, int ST, bool DBG, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
              const AttnArgs a) {
-  using P = SmemPlan<DP, ST>;
+  using P = SmemPlan<DP, ST, I8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const Geometry &g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the workspace must hold codes of this kernel's format (recorded by the prepass)
+  if (a.status[1] != (I8 ? kFormatInt8 : kFormatInt4)) {
+    if (tid == 0) atomicCAS(a.status, 0, kStatusFormat);
+    return;
+  }
 
   int b, hq, qt;
   if (DBG) {
@@ -272,11 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % ST;
         if (j >= ST && !mbar_wait<true>(&kv_empty[st], ((j / ST) - 1) & 1, ab, kSiteKvEmpty)) break;
         if (skip) continue;
-        mbar_arrive_expect_tx(&kv_full[st], 128 * DP + DP * 128 + 512 + 16);
-        tma_load_2d(smem + P::kK + st * 128 * DP, &tm_k, 0, yk0 + j * kBKV, &kv_full[st]);
+        mbar_arrive_expect_tx(&kv_full[st], P::kKStage + DP * 128 + (I8 ? 0 : 512) + 16);
+        if (I8) {  // 64-channel blocks of fp16 codes: inner coordinate 64 h (128 bytes)
+#pragma unroll
+          for (int hb = 0; hb < DP / 64; ++hb)
+            tma_load_2d(smem + P::kK + st * P::kKStage + hb * 16384, &tm_k, 64 * hb,
+                        yk0 + j * kBKV, &kv_full[st]);
+        } else {
+          tma_load_2d(smem + P::kK + st * P::kKStage, &tm_k, 0, yk0 + j * kBKV, &kv_full[st]);
+        }
         tma_load_2d(smem + P::kV + st * DP * 128, &tm_v, s.kvpad0 + j * kBKV, hk * DP,
                     &kv_full[st]);
-        bulk_load(smem + P::kDsc + st * 512, dsc_row + (size_t)j * kBKV, 512, &kv_full[st]);
+        if (!I8)
+          bulk_load(smem + P::kDsc + st * 512, dsc_row + (size_t)j * kBKV, 512, &kv_full[st]);
         bulk_load(smem + P::kSk + st * 16, sk_row + j * (kBKV / kGK), 16, &kv_full[st]);
         issued = j + 1;
       }
@@ -294,11 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1)
              mbar_wait<true>(&kv_full[j % ST], (j / ST) & 1, ab, kSiteKvFull);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + (j % ST) * 128 * DP), DP);
+        if (I8) {  // fp16 codes, 16 channels (32 bytes, 8 TMEM columns of A) per MMA
+          const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + (j % ST) * P::kKStage), 128);
 #pragma unroll
-        for (int kk = 0; kk < DP / 32; ++kk)  // A = the Q codes in tensor memory
-          mma_e4m3_ts(tbase + kColS, tbase + kColQ + kk * 8, kdesc + (uint64_t)(kk * 2), idesc_qk,
-                      kk > 0);
+          for (int kk = 0; kk < DP / 16; ++kk)
+            mma_f16_ts(tbase + kColS, tbase + kColQ + kk * 8,
+                       kdesc + (uint64_t)((kk & 3) * 2 + (kk >> 2) * (16384 >> 4)), idesc_qk,
+                       kk > 0);
+        } else {
+          const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + (j % ST) * P::kKStage), DP);
+#pragma unroll
+          for (int kk = 0; kk < DP / 32; ++kk)  // A = the Q codes in tensor memory
+            mma_e4m3_ts(tbase + kColS, tbase + kColQ + kk * 8, kdesc + (uint64_t)(kk * 2),
+                        idesc_qk, kk > 0);
+        }
         mma_commit(s_full);
       }
       mma_commit(&drain[0]);  // every MMA issued above completes before tensor memory is freed
@@ -343,10 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t tS = tbase + lane_base + kColS;
     {  // the row's Q codes into tensor memory: the A operand of Q K^T
+      constexpr int kRowBytes = DP * (I8 ? 2 : 1);
       const uint4 *qrow = reinterpret_cast<const uint4 *>(
-          a.qcode + ((size_t)hq * a.L.Tq + s.qpad0 + qt * kBQ + row) * DP);
+          a.qcode + ((size_t)hq * a.L.Tq + s.qpad0 + qt * kBQ + row) * kRowBytes);
 #pragma unroll
-      for (int c = 0; c < DP / 32; ++c) {  // 32 bytes = 8 words per store
+      for (int c = 0; c < kRowBytes / 32; ++c) {  // 32 bytes = 8 words per store
         const uint4 u0 = __ldg(qrow + 2 * c), u1 = __ldg(qrow + 2 * c + 1);
         const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
         tmem_st8(tbase + lane_base + kColQ + 8 * c, w8);
@@ -416,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t vh[64];
 #pragma unroll
         for (int e = 0; e < 64; ++e) vh[e] = v[64 * h + e];
-        pmax = fmaxf(pmax, logits64(xh, vh, dsc + 64 * h, skv + 2 * h, sqc, lim - 64 * h));
+        pmax = fmaxf(pmax, logits64<!I8>(xh, vh, dsc + 64 * h, skv + 2 * h, sqc, lim - 64 * h));
 #pragma unroll
         for (int e = 0; e < 64; ++e) x[64 * h + e] = xh[e];
       }
@@ -574,41 +603,45 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D u8 tensor map: inner extent `inner` bytes, `rows` rows, box (box_inner x box_rows).
+// 2-D tensor map of 1- or 2-byte elements: inner extent `inner` elements, `rows` rows, box
+// (box_inner x box_rows) elements.
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-              uint32_t box_rows, CUtensorMapSwizzle sw) {
+              uint32_t box_rows, CUtensorMapSwizzle sw, int elem_bytes = 1) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner};
+  const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DP, int ST, bool DBG>
+template <int DP, int ST, bool DBG, bool I8>
 cudaError_t launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, dim3 grid,
                      cudaStream_t st) {
-  using P = SmemPlan<DP, ST>;
+  using P = SmemPlan<DP, ST, I8>;
   // at least 116 KB so that a single CTA occupies an SM (each allocates all 512 TMEM columns)
   constexpr int kSmem = P::kBytes > 116 * 1024 ? P::kBytes : 116 * 1024;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_fwd<DP, ST, DBG>,
+    attr_err = cudaFuncSetAttribute(attn_fwd<DP, ST, DBG, I8>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attn_fwd<DP, ST, DBG><<<grid, kThreads, kSmem, st>>>(mk, mv, a);
+  attn_fwd<DP, ST, DBG, I8><<<grid, kThreads, kSmem, st>>>(mk, mv, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const Layout &L,
-                             const void *ws, cudaStream_t st, const AttnDebug *dbg) {
+                             const void *ws, cudaStream_t st, const AttnDebug *dbg, bool int8_qk) {
+  if (int8_qk != (L.code_bytes == 2)) return cudaErrorInvalidValue;
   const WsPtrs w = ws_ptrs(const_cast<void *>(ws), L);
   AttnArgs a;
   a.g = g;
@@ -625,18 +658,30 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
   const CUtensorMapSwizzle qk_sw =
       g.Dp == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap mk, mv;
-  if (!make_map(&mk, w.kcode, g.Dp, (uint64_t)g.Hkv * L.Tkv, g.Dp, 128, qk_sw) ||
-      !make_map(&mv, w.vcodeT, L.Tkv, (uint64_t)g.Hkv * g.Dp, 128, g.Dp,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+  // INT8 path: fp16 codes in 64-channel boxes (128-byte swizzled rows), DP / 64 per tile
+  const bool mk_ok = int8_qk ? make_map(&mk, w.kcode, g.Dp, (uint64_t)g.Hkv * L.Tkv, 64, 128,
+                                        CU_TENSOR_MAP_SWIZZLE_128B, 2)
+                             : make_map(&mk, w.kcode, g.Dp, (uint64_t)g.Hkv * L.Tkv, g.Dp, 128, qk_sw);
+  if (!mk_ok || !make_map(&mv, w.vcodeT, L.Tkv, (uint64_t)g.Hkv * g.Dp, 128, g.Dp,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int nqt = (g.max_nq + kBQ - 1) / kBQ;
-  if (dbg) {
-    if (g.Dp == 128) return launch_t<128, 6, true>(mk, mv, a, dim3(1), st);
-    return launch_t<64, 8, true>(mk, mv, a, dim3(1), st);
+  const dim3 grid = dbg ? dim3(1) : dim3(nqt, g.Hq, g.B);
+  // pipeline depth: as many K/V stages as fit (a stage of fp16 K codes is twice as large)
+  if (int8_qk) {
+    if (dbg) {
+      if (g.Dp == 128) return launch_t<128, 4, true, true>(mk, mv, a, grid, st);
+      return launch_t<64, 8, true, true>(mk, mv, a, grid, st);
+    }
+    if (g.Dp == 128) return launch_t<128, 4, false, true>(mk, mv, a, grid, st);
+    return launch_t<64, 8, false, true>(mk, mv, a, grid, st);
   }
-  const dim3 grid(nqt, g.Hq, g.B);
-  if (g.Dp == 128) return launch_t<128, 6, false>(mk, mv, a, grid, st);
-  return launch_t<64, 8, false>(mk, mv, a, grid, st);
+  if (dbg) {
+    if (g.Dp == 128) return launch_t<128, 6, true, false>(mk, mv, a, grid, st);
+    return launch_t<64, 8, true, false>(mk, mv, a, grid, st);
+  }
+  if (g.Dp == 128) return launch_t<128, 6, false, false>(mk, mv, a, grid, st);
+  return launch_t<64, 8, false, false>(mk, mv, a, grid, st);
 }
 
 }  // namespace sage2

@@ -21,6 +21,7 @@ namespace sage2 {
 enum : int {
   kStatusTimeoutBase = 0x100,  // | wait site id
   kStatusSeqTooLong = 0x200,   // varlen sequence longer than the declared maximum
+  kStatusFormat = 0x300,       // workspace prepared for the other code format (INT4 / INT8)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -191,6 +192,16 @@ __device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, ui
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// kind::f16 with A in tensor memory: A = B = f16, D = f32, K = 16 per instruction. The
+// instruction descriptor has the same bit layout as idesc_e4m3_f32 (format 0 is f16 here).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

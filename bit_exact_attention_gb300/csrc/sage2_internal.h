@@ -30,11 +30,18 @@ struct Layout {
   size_t qcode, kcode, vcodeT, qscale, kscale, qmean, kmean, vscale, vinv, dsc, kpart, vpart,
       status;
   int Tq, Tkv, nqblk, nkv_pad, nchunk;
+  int code_bytes;  // bytes per Q / K code: 1 (INT4 grid as e4m3), 2 (INT8 grid as fp16)
 };
 
 // Computes the workspace layout; returns false on sizes that overflow or are invalid.
+// code_bytes: 1 for the method's INT4-grid codes, 2 for the INT8-grid codes (fp16 values).
 bool make_layout(int B, int Hq, int Hkv, int max_nq, int max_nkv, int Dp, int total_q,
-                 int total_kv, Layout *L);
+                 int total_kv, int code_bytes, Layout *L);
+
+// Code format a prepass leaves in word 1 of the workspace status area (every byte of the word
+// the same), checked by the attention kernel before it reads anything else.
+constexpr unsigned char kFormatInt4Byte = 0x34, kFormatInt8Byte = 0x38;
+constexpr int kFormatInt4 = 0x34343434, kFormatInt8 = 0x38383838;
 
 // Pointers into a workspace.
 struct WsPtrs {
@@ -102,7 +109,10 @@ struct AttnDebug {
   float *r_out;            // [128][Dp]
   int skip_loads;          // producer issues nothing: every wait must time out
 };
+// int8_qk: the INT8-grid variant (Q K^T on fp16 codes); the workspace must come from a prepass
+// with SAGE2_QUANT_SAGE1, and the other way round (checked on the device).
 cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const Layout &L,
-                             const void *ws, cudaStream_t st, const AttnDebug *dbg);
+                             const void *ws, cudaStream_t st, const AttnDebug *dbg,
+                             bool int8_qk = false);
 
 }  // namespace sage2

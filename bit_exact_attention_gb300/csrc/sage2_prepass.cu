@@ -74,6 +74,13 @@ __device__ __forceinline__ float int4_code(float x, float inv) {
   return __fadd_rn(r, 0.f);
 }
 
+// Code of x * inv on the grid [-G, G] as a float (canonical +0 for zero).
+__device__ __forceinline__ float grid_code(float x, float inv, float G) {
+  float r = rintf(__fmul_rn(x, inv));
+  r = fminf(fmaxf(r, -G), G);
+  return __fadd_rn(r, 0.f);
+}
+
 __device__ __forceinline__ void flag_bad_seq(int *status) {
   atomicCAS(status, 0, kStatusSeqTooLong);
 }
@@ -183,9 +190,10 @@ __global__ void __launch_bounds__(kFinalThreads) kv_stats_final(PrepassArgs a) {
 // memory with asynchronous 16-byte copies (rows past the end and channels past D0 read as 0);
 // warp w handles keys 16w .. 16w + 15, i.e. half of the 32-key scale group w / 2; lane l
 // channels [l * CPL, l * CPL + CPL). Per-block switch: the eight warps share one maximum.
-template <int DP, bool BF16>
+template <int DP, bool BF16, bool I8>
 __global__ void __launch_bounds__(256) k_quant(PrepassArgs a) {
   constexpr int CPL = DP / 32, RPW = 16;
+  constexpr float G = I8 ? 127.f : 7.f;  // the code grid [-G, G]
   __shared__ __align__(16) uint16_t blk[kBKV][DP];
   __shared__ float wmax[kBKV / RPW];
   const Geometry &g = a.g;
@@ -234,12 +242,24 @@ __global__ void __launch_bounds__(256) k_quant(PrepassArgs a) {
   } else {
     amax = fmaxf(wmax[warp & ~1], wmax[warp | 1]);  // the two halves of the 32-key group
   }
-  const float inv = amax > 0.f ? __fdiv_rn(7.f, amax) : 0.f;
-  const float scale = amax > 0.f ? __fdiv_rn(amax, 7.f) : 0.f;
-  uint8_t *dst = a.w.kcode + ((size_t)h * a.L.Tkv + s.kvpad0 + tile * kBKV + rbase) * DP + c0;
+  const float inv = amax > 0.f ? __fdiv_rn(G, amax) : 0.f;
+  const float scale = amax > 0.f ? __fdiv_rn(amax, G) : 0.f;
+  const size_t e0 = ((size_t)h * a.L.Tkv + s.kvpad0 + tile * kBKV + rbase) * DP + c0;
+  uint8_t *dst = a.w.kcode + e0;
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
-    if (CPL == 4) {
+    if (I8) {  // INT8-grid codes as fp16 values (exact), two bytes each
+      uint16_t hv[CPL];
+#pragma unroll
+      for (int e = 0; e < CPL; ++e)
+        hv[e] = __half_as_ushort(__float2half_rn(grid_code(smoothed(r, e), inv, G)));
+      uint16_t *d16 = reinterpret_cast<uint16_t *>(a.w.kcode) + e0 + (size_t)r * DP;
+      if (CPL == 4)
+        *reinterpret_cast<uint2 *>(d16) = make_uint2(hv[0] | ((uint32_t)hv[1] << 16),
+                                                     hv[2] | ((uint32_t)hv[3] << 16));
+      else
+        *reinterpret_cast<uint32_t *>(d16) = hv[0] | ((uint32_t)hv[1] << 16);
+    } else if (CPL == 4) {
       const uint32_t lo = cvt_e4m3x2(int4_code(smoothed(r, 0), inv), int4_code(smoothed(r, 1), inv));
       const uint32_t hi = cvt_e4m3x2(int4_code(smoothed(r, 2), inv), int4_code(smoothed(r, 3), inv));
       *reinterpret_cast<uint32_t *>(dst + (size_t)r * DP) = lo | (hi << 16);
@@ -306,9 +326,10 @@ __global__ void __launch_bounds__(256) v_quant(PrepassArgs a) {
 // double. The sums are exact for 16-bit inputs, so the mean is the definition's fl32(sum / n).
 // Quantization: warp w owns rows 16w .. 16w + 15, lane l channels [l * CPL, l * CPL + CPL), all
 // elementwise steps on packed FP32 pairs (each lane of a pair rounds like the scalar form).
-template <int DP, bool BF16>
+template <int DP, bool BF16, bool I8>
 __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
   constexpr int CPL = DP / 32, RPW = 16;
+  constexpr float G = I8 ? 127.f : 7.f;  // the code grid [-G, G]
   constexpr int kPairs = DP / 2, kParts = 256 / kPairs, kRowsPer = kBQ / kParts;
   __shared__ __align__(16) uint16_t blk[kBQ][DP];  // rows past the end / channels past D0: 0
   __shared__ double colsum[kParts][DP];
@@ -420,9 +441,9 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
     rmax = rbase + (lane >> 1) < nvalid ? m : 0.f;
   }
   // one division per lane (row lane >> 1); rows past the end have rmax = 0: codes and scale 0
-  const float inv_mine = rmax > 0.f ? __fdiv_rn(7.f, rmax) : 0.f;
+  const float inv_mine = rmax > 0.f ? __fdiv_rn(G, rmax) : 0.f;
   const size_t row0 = (size_t)h * a.L.Tq + s.qpad0 + qb * kBQ + rbase;
-  if ((lane & 1) == 0) a.w.qscale[row0 + (lane >> 1)] = rmax > 0.f ? __fdiv_rn(rmax, 7.f) : 0.f;
+  if ((lane & 1) == 0) a.w.qscale[row0 + (lane >> 1)] = rmax > 0.f ? __fdiv_rn(rmax, G) : 0.f;
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     float x[CPL];
@@ -433,16 +454,27 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
     for (int e = 0; e < CPL; e += 2) mul2(t[e], t[e + 1], x[e], x[e + 1], inv, inv);
 #pragma unroll
     for (int e = 0; e < CPL; ++e) t[e] = rintf(t[e]);
-    // |x| <= rmax and inv = fl32(7 / rmax) give |fl32(x * inv)| <= 7 whenever inv is finite;
-    // only an overflowed inv (rmax below 7 / FLT_MAX) needs the clamp to [-7, 7]
+    // |x| <= rmax and inv = fl32(G / rmax) give |fl32(x * inv)| <= G whenever inv is finite
+    // (G(1 + 2^-24) rounds to G for G = 7 and 127); only an overflowed inv (rmax below
+    // G / FLT_MAX) needs the clamp to [-G, G]
     if (__builtin_expect(isinf(inv), 0)) {
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) t[e] = fminf(fmaxf(t[e], -7.f), 7.f);
+      for (int e = 0; e < CPL; ++e) t[e] = fminf(fmaxf(t[e], -G), G);
     }
 #pragma unroll
     for (int e = 0; e < CPL; e += 2) add2(t[e], t[e + 1], t[e], t[e + 1], 0.f, 0.f);  // +0 for -0
     uint8_t *dst = a.w.qcode + (row0 + r) * DP + c0;
-    if (CPL == 4) {
+    if (I8) {  // INT8-grid codes as fp16 values (exact), two bytes each
+      uint16_t *d16 = reinterpret_cast<uint16_t *>(a.w.qcode) + (row0 + r) * DP + c0;
+      uint16_t hv[CPL];
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) hv[e] = __half_as_ushort(__float2half_rn(t[e]));
+      if (CPL == 4)
+        *reinterpret_cast<uint2 *>(d16) = make_uint2(hv[0] | ((uint32_t)hv[1] << 16),
+                                                     hv[2] | ((uint32_t)hv[3] << 16));
+      else
+        *reinterpret_cast<uint32_t *>(d16) = hv[0] | ((uint32_t)hv[1] << 16);
+    } else if (CPL == 4) {
       *reinterpret_cast<uint32_t *>(dst) = cvt_e4m3x2(t[0], t[1]) | (cvt_e4m3x2(t[2], t[3]) << 16);
     } else {
       *reinterpret_cast<uint16_t *>(dst) = (uint16_t)cvt_e4m3x2(t[0], t[1]);
@@ -631,11 +663,15 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   a.k = static_cast<const uint16_t *>(k);
   a.v = static_cast<const uint16_t *>(v);
   const bool bf16 = in_dtype == SAGE2_BF16;
-  a.flags = quant_flags;
+  const bool int8 = (quant_flags & SAGE2_QUANT_SAGE1) != 0;
+  a.flags = int8 ? (SAGE2_QUANT_NO_SMOOTH_Q | SAGE2_QUANT_PER_BLOCK) : quant_flags;
   a.g = g;
   a.L = L;
   a.w = ws_ptrs(ws, L);
   cudaError_t e = cudaMemsetAsync(a.w.status, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  // the code format, checked by the attention kernel
+  e = cudaMemsetAsync(a.w.status + 1, int8 ? kFormatInt8Byte : kFormatInt4Byte, sizeof(int), st);
   if (e != cudaSuccess) return e;
 
   const int nvec = g.Hkv * g.D0 / 8;
@@ -655,14 +691,19 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   const dim3 ds_grid((max(1, g.max_nkv) + ds_keys - 1) / ds_keys,
                      (max_rows + ds_rows - 1) / ds_rows, g.B * g.Hkv);
   // kernels instantiated per padded head dim and input type
-  auto run = [&](auto dp_tag, auto bf_tag) {
+  // kernels instantiated per padded head dim, input type and code grid. The INT8 path (the
+  // SageAttention (v1) switch) has per-block scales, no Q smoothing and so no DeltaS: the
+  // attention kernel for it reads none.
+  auto run = [&](auto dp_tag, auto bf_tag, auto i8_tag) {
     constexpr int DP = decltype(dp_tag)::value;
     constexpr bool BF = decltype(bf_tag)::value;
+    constexpr bool I8 = decltype(i8_tag)::value;
     kv_stats_partial<BF><<<stat_grid, kStatThreads, 0, st>>>(a);
     kv_stats_final<<<dim3(g.B * g.Hkv, g.Dp / kFinalChan), kFinalThreads, 0, st>>>(a);
-    k_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
+    k_quant<DP, BF, I8><<<kv_grid, 256, 0, st>>>(a);
     v_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
-    q_quant<DP, BF><<<q_grid, 256, 0, st>>>(a);
+    q_quant<DP, BF, I8><<<q_grid, 256, 0, st>>>(a);
+    if (I8) return;
     if (ds_rows == 128)
       delta_s<DP, 128, BF><<<ds_grid, 256, 0, st>>>(a);
     else if (ds_rows == 64)
@@ -670,15 +711,19 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
     else
       delta_s<DP, 32, BF><<<ds_grid, 256, 0, st>>>(a);
   };
-  using T128 = std::integral_constant<int, 128>;
-  using T64 = std::integral_constant<int, 64>;
-  if (g.Dp == 128) {
-    if (bf16) run(T128(), std::true_type());
-    else run(T128(), std::false_type());
-  } else {
-    if (bf16) run(T64(), std::true_type());
-    else run(T64(), std::false_type());
-  }
+  auto run_dp = [&](auto i8_tag) {
+    using T128 = std::integral_constant<int, 128>;
+    using T64 = std::integral_constant<int, 64>;
+    if (g.Dp == 128) {
+      if (bf16) run(T128(), std::true_type(), i8_tag);
+      else run(T128(), std::false_type(), i8_tag);
+    } else {
+      if (bf16) run(T64(), std::true_type(), i8_tag);
+      else run(T64(), std::false_type(), i8_tag);
+    }
+  };
+  if (int8) run_dp(std::true_type());
+  else run_dp(std::false_type());
   return cudaGetLastError();
 }
 

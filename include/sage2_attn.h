@@ -116,23 +116,51 @@ int sage2_attention_varlen(void *out, int out_dtype, const int *cu_seqlens_q,
 typedef enum {
   SAGE2_QUANT_NO_SMOOTH_Q = 1, /* Q block mean taken as 0: Q~ = Q and DeltaS = 0 */
   SAGE2_QUANT_NO_SMOOTH_K = 2, /* K channel mean taken as 0: K~ = K */
-  SAGE2_QUANT_PER_BLOCK = 4    /* one INT4 scale per 128-row Q block and per 128-key K block
+  SAGE2_QUANT_PER_BLOCK = 4,   /* one INT4 scale per 128-row Q block and per 128-key K block
                                   (instead of one per query row and per 32 keys) */
+  SAGE2_QUANT_SAGE1 = 8        /* the SageAttention (v1) path the research note contrasts the
+                                  method with (its opening paragraph): Q and K codes on the INT8
+                                  grid [-127, 127], one scale per 128-row Q block and per 128-key
+                                  K block, K smoothed, Q not (no DeltaS); P~ and V as in the
+                                  method. Q K^T runs on 16-bit tensor-core operands holding the
+                                  integer codes exactly. Must be used alone; it changes the
+                                  workspace size (two bytes per Q and K code) and the attention
+                                  kernel, so the workspace, prepass and attention calls must all
+                                  be given it. */
 } sage2_quant_flags;
 
-/* sage2_prepass_varlen with quantization switches (an OR of sage2_quant_flags; other bits
- * return SAGE2_EINVAL). Same arguments, workspace contents and errors otherwise; follow it
- * with sage2_attention_varlen on the same workspace. */
+/* Workspace size and layout for a quantization setting (sage2_quant_flags; 0 gives
+ * sage2_workspace_size / sage2_workspace_layout). 0 / SAGE2_EINVAL on invalid arguments. */
+size_t sage2_workspace_size_ex(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D,
+                               int total_q, int total_kv, int quant_flags);
+
+/* sage2_prepass_varlen with quantization switches (sage2_quant_flags: the first three in any
+ * combination, or SAGE2_QUANT_SAGE1 alone; anything else returns SAGE2_EINVAL). Same arguments,
+ * workspace contents and errors otherwise; the workspace must hold
+ * sage2_workspace_size_ex(..., quant_flags) bytes. Follow it with sage2_attention_varlen_ex
+ * (same quant_flags) on the same workspace. The prepass records the code format in the
+ * workspace; an attention call for the other format finds it there, writes nothing and makes
+ * sage2_device_status return SAGE2_EINVAL. */
 int sage2_prepass_varlen_ex(const void *q, const void *k, const void *v, int in_dtype,
                             const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq,
                             int Hkv, int max_Nq, int max_Nkv, int total_q, int total_kv, int D,
                             int causal, float sm_scale, int quant_flags, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* sage2_attention_varlen for a workspace filled by sage2_prepass_varlen_ex with the same
+ * quant_flags (only SAGE2_QUANT_SAGE1 selects another kernel; the other switches only change
+ * what the prepass wrote). */
+int sage2_attention_varlen_ex(void *out, int out_dtype, const int *cu_seqlens_q,
+                              const int *cu_seqlens_kv, int B, int Hq, int Hkv, int max_Nq,
+                              int max_Nkv, int total_q, int total_kv, int D, int causal,
+                              float sm_scale, int quant_flags, const void *workspace,
+                              size_t workspace_bytes, void *stream);
+
 /* Synchronizes `stream`, then reads the workspace's device status word (cleared by every
  * prepass). Returns SAGE2_OK, SAGE2_EDEVICE_TIMEOUT (a bounded wait expired) or
- * SAGE2_EINVAL (a varlen sequence exceeded max_Nq/max_Nkv); *raw (if not NULL) receives
- * the word itself (0 when clean; otherwise a code naming the wait that gave up). */
+ * SAGE2_EINVAL (a varlen sequence exceeded max_Nq/max_Nkv, or the attention call's code format
+ * was not the one its prepass wrote); *raw (if not NULL) receives the word itself (0 when clean;
+ * otherwise a code naming the wait that gave up). */
 int sage2_device_status(const void *workspace, void *stream, int *raw);
 
 /* Byte offsets of the buffers inside a workspace, for tests and tools that read the
@@ -150,10 +178,14 @@ typedef struct {
   size_t qcode, kcode, vcodeT, qscale, kscale, qmean, kmean, vscale, vinv, dsc;
   size_t kpart, vpart, status;
   int Dp, Tq, Tkv, nkv_pad, nchunk;
+  int code_bytes; /* bytes per Q and K code: 1 (e4m3 byte), 2 (SAGE2_QUANT_SAGE1: fp16 value) */
 } sage2_ws_layout;
 
 int sage2_workspace_layout(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D, int total_q,
                            int total_kv, sage2_ws_layout *layout);
+int sage2_workspace_layout_ex(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, int D,
+                              int total_q, int total_kv, int quant_flags,
+                              sage2_ws_layout *layout);
 
 /* Test hook (unstable): reruns the attention kernel for the single (sequence b, q head h,
  * q tile qt) work unit on a prepared workspace and dumps, for its KV tile kt, the raw
@@ -165,6 +197,12 @@ int sage2_debug_tile(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, i
                      int max_Nq, int max_Nkv, int total_q, int total_kv, int D, int causal,
                      float sm_scale, const void *workspace, size_t workspace_bytes, int b, int h,
                      int qt, int kt, float *s_out, uint8_t *p_out, float *r_out, void *stream);
+/* sage2_debug_tile for a workspace prepared with quant_flags (see sage2_prepass_varlen_ex). */
+int sage2_debug_tile_ex(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq,
+                        int Hkv, int max_Nq, int max_Nkv, int total_q, int total_kv, int D,
+                        int causal, float sm_scale, int quant_flags, const void *workspace,
+                        size_t workspace_bytes, int b, int h, int qt, int kt, float *s_out,
+                        uint8_t *p_out, float *r_out, void *stream);
 
 /* Test hook (unstable): runs one attention work unit whose producer never issues its
  * loads, so every consumer wait must expire (about one second); the kernel must return on

@@ -31,7 +31,8 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import GpuRun, bits, c32_of, kv_tiles, metrics, pad_starts
+from parity_util import (GpuRun, bits, c32_of, check_forward_with_flips, compare_p_codes, kv_tiles,
+                         metrics, pad_starts)
 
 pytestmark = pytest.mark.gpu
 
@@ -80,9 +81,11 @@ def test_flag_word_and_invalid_bits():
     assert S.quant_flags() == 0
     assert S.quant_flags(smooth_q=False, smooth_k=False, per_block=True) == 7
     w, x = _case("prefill")
-    g = GpuRun(w, x, quant_flags=8)
-    with pytest.raises(S.Sage2Error):
-        g.prepass()
+    g = GpuRun(w, x)
+    for bad in (16, S.QUANT_SAGE1 | S.QUANT_PER_BLOCK):  # an unknown bit; SAGE1 combined
+        g.quant_flags = bad
+        with pytest.raises(S.Sage2Error):
+            g.prepass()
 
 
 @pytest.mark.parametrize("setting", [s for s in SETTINGS if s != "method"])
@@ -130,34 +133,7 @@ def test_p_codes_agree_except_at_exp2_rounding_midpoints(name, setting):
     w, x = _case(name)
     g = GpuRun(w, x, quant_flags=S.quant_flags(**kw))
     g.prepass()
-    n_cmp = n_diff = 0
-    for b in range(w.batch):
-        nqb = (w.nq[b] + 127) // 128
-        for (h, qt) in sorted({(0, 0), (w.hq - 1, nqb - 1), (w.hq // 2, nqb // 2)}):
-            if nqb == 0:
-                continue
-            T = kv_tiles(qt, w.nq[b], w.nkv[b], w.causal)
-            for kt in sorted({0, T // 2, T - 1}):
-                if kt < 0:
-                    continue
-                _, p_out, _ = g.debug_tile(b, h, qt, kt)
-                nr = min(128, w.nq[b] - qt * 128)
-                got = p_out.cpu().numpy()[:nr]
-                p448 = oracle.emulated_tile_p448(*_args(w, x), b, h, qt, kt, **kw)[:nr]
-                want = oracle.e4m3_encode(p448.astype(np.float64))
-                diff = got != want
-                n_cmp += got.size
-                n_diff += int(diff.sum())
-                if diff.any():
-                    # positive e4m3 bytes are ordered like their values: one step = one byte
-                    step = np.abs(got[diff].astype(np.int64) - want[diff].astype(np.int64))
-                    assert np.all(step == 1), f"b{b} h{h} qt{qt} kt{kt}: codes more than one step off"
-                    lo = oracle.e4m3_decode(np.minimum(got[diff], want[diff]))
-                    hi = oracle.e4m3_decode(np.maximum(got[diff], want[diff]))
-                    mid = (lo + hi) / 2
-                    ulp = np.spacing(mid.astype(np.float32)).astype(np.float64)
-                    off = np.abs(p448[diff].astype(np.float64) - mid) / ulp
-                    assert off.max() <= 4, f"b{b} h{h} qt{qt} kt{kt}: a code flip {off.max()} ulp from a midpoint"
+    n_diff, n_cmp = compare_p_codes(g, w, x, kw)
     assert n_diff <= 1e-3 * n_cmp, (n_diff, n_cmp)
 
 
@@ -198,16 +174,6 @@ def test_pv_tile_accumulator_is_fp32_class():
     assert worst <= 2.0 ** -19, np.log2(worst)
 
 
-def _check_forward(out, emu, x):
-    m = metrics(out, emu)
-    assert m["relL1"] <= REL_L1, m
-    vmax = float(np.abs(x["v"].double().numpy()).max())
-    d = np.abs(out - emu)
-    assert d.max() <= vmax / 8 + MAX_ABS, (d.max(), vmax)
-    rows_off = int((d.reshape(-1, d.shape[-1]).max(axis=1) > MAX_ABS).sum())
-    assert rows_off <= max(2, d.shape[0] * d.shape[1] // 100), rows_off
-
-
 @pytest.mark.parametrize("setting", list(SETTINGS))
 @pytest.mark.parametrize("name", list(CASES))
 def test_forward_matches_emulation_with_switches(name, setting):
@@ -217,7 +183,7 @@ def test_forward_matches_emulation_with_switches(name, setting):
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle.attention_emulated(*_args(w, x), **kw)
-    _check_forward(out, emu, x)
+    check_forward_with_flips(out, emu, x)
 
 
 def test_dense_entry_with_switches_equals_varlen():
