@@ -48,15 +48,19 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # DRAM bytes (read + write) of one attention launch, from a one-pass ncu capture of
 # dram__bytes_read.sum / dram__bytes_write.sum on the full workload (profiles/), valid only for
 # the kernel source they were taken on (sha256 prefix of csrc/sage2_attention.cu).
-MEASURED_TRAFFIC = {"gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16": (
-    "f8a1998b174b0677", 745.57e6 + 246.42e6)}
+MEASURED_TRAFFIC = {
+    ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage2"): (
+        "74c005a605d43bd1", 745.38e6 + 246.30e6),
+    ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage1"): (
+        "74c005a605d43bd1", 374.60e6 + 233.44e6),
+}
 
 
-def measured_traffic(w):
-    """The captured DRAM bytes per attention launch for this workload, or None when there is
-    none or the kernel source has changed since the capture."""
+def measured_traffic(w, quant="sage2"):
+    """The captured DRAM bytes per attention launch for this workload and path, or None when
+    there is none or the kernel source has changed since the capture."""
     import hashlib
-    rec = MEASURED_TRAFFIC.get(w.name)
+    rec = MEASURED_TRAFFIC.get((w.name, quant))
     if rec is None:
         return None
     src = os.path.join(ROOT, "bit_exact_attention_gb300", "csrc", "sage2_attention.cu")
@@ -74,6 +78,9 @@ def parse():
     p.add_argument("--workload", default="gqa_long", choices=sorted(WORKLOADS))
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--quant", default="sage2", choices=["sage2", "sage1"],
+                   help="sage2: the method (INT4-grid Q, K); sage1: the SageAttention (v1) "
+                        "path (INT8 per-block Q, K on 16-bit tensor-core operands)")
     return p.parse_args()
 
 
@@ -190,13 +197,15 @@ def oracle_sample(w: W.Workload, x: dict, n_units: int, seed: int = 0):
     return units, ops
 
 
-def run_oracle_sample(w: W.Workload, x: dict, units):
+def run_oracle_sample(w: W.Workload, x: dict, units, quant="sage2"):
     import oracle
     oracle.build()
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    kw = oracle.SAGE1 if quant == "sage1" else {}
     t0 = time.perf_counter()
     oracle.attention_emulated(bits(x["q"]), bits(x["k"]), bits(x["v"]), W.dtype_code(w),
-                              x["cu_q"], x["cu_kv"], w.hq, w.hkv, w.d, w.causal, units=units)
+                              x["cu_q"], x["cu_kv"], w.hq, w.hkv, w.d, w.causal, units=units,
+                              **kw)
     return time.perf_counter() - t0, oracle.num_threads()
 
 
@@ -219,18 +228,21 @@ def run_ours(args, rank, world, local):
     cu_q = torch.tensor(x["cu_q"], dtype=torch.int32, device=dev)
     cu_kv = torch.tensor(x["cu_kv"], dtype=torch.int32, device=dev)
     out = torch.empty(tq, hq, d, dtype=q.dtype, device=dev)
-    nws = S.workspace_size(B, hq, hkv, max_nq, max_nkv, d, tq, tkv)
+    sage1 = args.quant == "sage1"
+    qf = S.QUANT_SAGE1 if sage1 else 0
+    nws = S.workspace_size(B, hq, hkv, max_nq, max_nkv, d, tq, tkv, quant_flags=qf)
     ws = S.alloc_workspace(nws, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ops = w.metric_ops()
 
     def prepass():
-        S.prepass_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, ws, causal=w.causal, stream=stream)
+        S.prepass_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, ws, causal=w.causal, stream=stream,
+                         quant_flags=qf)
 
     def attention():
         S.attention_varlen(out, ws, cu_q, cu_kv, hkv, max_nq, max_nkv, tkv, causal=w.causal,
-                           stream=stream)
+                           stream=stream, quant_flags=qf)
 
     for _ in range(args.warmup):
         prepass()
@@ -268,7 +280,7 @@ def run_ours(args, rank, world, local):
     ms_per_step = total_s * 1e3 / args.steps
     att_mean = statistics.mean(att_ms)
     pre_mean = statistics.mean(pre_ms)
-    kernels_per_step = 7  # prepass: 6 kernels; attention: 1
+    kernels_per_step = 6 if sage1 else 7  # prepass: 6 kernels (5 without DeltaS); attention: 1
 
     # end to end through the public API: pinned host inputs in, host output back
     e2e = None
@@ -280,7 +292,7 @@ def run_ours(args, rank, world, local):
             k.copy_(hk_, non_blocking=True)
             v.copy_(hv_, non_blocking=True)
             S.attn_fwd_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, causal=w.causal, out=out,
-                              workspace=ws, stream=stream)
+                              workspace=ws, stream=stream, quant_flags=qf)
             hout.copy_(out, non_blocking=True)
         torch.cuda.synchronize(dev)
         es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -293,7 +305,7 @@ def run_ours(args, rank, world, local):
             k.copy_(hk_, non_blocking=True)
             v.copy_(hv_, non_blocking=True)
             S.attn_fwd_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, causal=w.causal, out=out,
-                              workspace=ws, stream=stream)
+                              workspace=ws, stream=stream, quant_flags=qf)
             hout.copy_(out, non_blocking=True)
             es[i][1].record(stream)
         torch.cuda.synchronize(dev)
@@ -306,17 +318,24 @@ def run_ours(args, rank, world, local):
                "ms_per_step": e2e_s * 1e3 / args.steps}
 
     bf16_burst, bf16_sust, peak_src = measured_peaks()
-    peak = bf16_burst * FP8_OVER_BF16
+    # sage2: both MMAs on e4m3 (the FP8 rate); sage1: Q K^T on 16-bit operands (the bf16 rate)
+    # and P~V on e4m3 for equal op counts, so the roofline is the time-weighted
+    # 2 / (1 / P16 + 1 / P8) = 4/3 of the 16-bit rate
+    mix = (2.0 / (1.0 + 1.0 / FP8_OVER_BF16)) if sage1 else FP8_OVER_BF16
+    peak = bf16_burst * mix
     achieved = ops / (att_mean / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": measured_traffic(w),
-                "kernel": "attn_fwd", "peak_source": f"{peak_src} bf16 burst x {FP8_OVER_BF16} (e4m3)",
-                "frac_of_sustained": round(achieved / (bf16_sust * FP8_OVER_BF16), 4)}
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": measured_traffic(w, args.quant), "kernel": "attn_fwd",
+                "peak_source": (f"{peak_src} bf16 burst x {mix:.4g} (Q K^T f16, P~V e4m3, "
+                                "time-weighted)" if sage1 else
+                                f"{peak_src} bf16 burst x {FP8_OVER_BF16} (e4m3)"),
+                "frac_of_sustained": round(achieved / (bf16_sust * mix), 4)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         units, sops = oracle_sample(w, x, sample_size(w))
-        secs, cores = run_oracle_sample(w, x, units)
+        secs, cores = run_oracle_sample(w, x, units, args.quant)
         cpu = {"value": sops / secs / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
                "sample": f"{len(units)} seeded (sequence, head, 128-row Q block) units of "
                          f"{w.name} ({sops:.3e} ops); the oracle's quantization of the full "
@@ -326,12 +345,14 @@ def run_ours(args, rank, world, local):
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16+e4m3" if sage1 else "e4m3",
             "data": "synthetic (seeded, distributions of the workload description)",
             "config": {"workload": w.name, "batch": B, "hq": hq, "hkv": hkv, "nq": list(w.nq),
                        "nkv": list(w.nkv), "d": d, "causal": w.causal, "in_dtype": w.dtype,
                        "metric_ops_per_step": ops, "parallelism": f"replicas x{world}",
-                       "l2": "flushed between timed steps (256 MB write)"},
+                       "l2": "flushed between timed steps (256 MB write)",
+                       **({"quant": "sage1 (INT8 per-block Q, K; K smoothed)"} if sage1 else {})},
             "kernel_only_tops": round(ops / (att_mean / 1e3) / 1e12, 3),
             "prepass_ms": round(pre_mean, 4), "attention_ms": round(att_mean, 4),
             "wall_s": round(t_wall, 4),
@@ -350,10 +371,10 @@ def run_reference(args, rank, world):
     x = W.make_inputs(w)
     units, sops = oracle_sample(w, x, max(2, sample_size(w) // 4))
     for _ in range(args.warmup):  # untimed, on a single unit to keep the run short
-        run_oracle_sample(w, x, units[:1])
+        run_oracle_sample(w, x, units[:1], args.quant)
     times, cores = [], 1
     for i in range(args.steps):
-        s, cores = run_oracle_sample(w, x, units)
+        s, cores = run_oracle_sample(w, x, units, args.quant)
         times.append(s)
     total = sum(times)
     value = sops * args.steps / total / 1e12

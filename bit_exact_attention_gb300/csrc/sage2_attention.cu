@@ -185,11 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const Geometry &g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // the workspace must hold codes of this kernel's format (recorded by the prepass)
-  if (a.status[1] != (I8 ? kFormatInt8 : kFormatInt4)) {
-    if (tid == 0) atomicCAS(a.status, 0, kStatusFormat);
-    return;
-  }
+  // the code format recorded by the prepass (loaded together with the sequence bounds below)
+  const int format = a.status[1];
 
   int b, hq, qt;
   if (DBG) {
@@ -202,6 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     qt = g.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
   }
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
+  if (format != (I8 ? kFormatInt8 : kFormatInt4)) {  // a workspace of the other code format
+    if (tid == 0) atomicCAS(a.status, 0, kStatusFormat);
+    return;
+  }
   if (!s.ok || qt * kBQ >= s.nq) return;
   const int hk = hq / (g.Hq / g.Hkv);
   const int T = kv_tiles_for(qt, s.nq, s.nkv, g.causal);
