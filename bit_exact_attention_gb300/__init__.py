@@ -23,7 +23,8 @@ __all__ = ["attn_fwd", "attn_fwd_varlen", "prepass", "attention", "prepass_varle
            "attention_varlen", "workspace_size", "workspace_layout", "device_status",
            "alloc_workspace", "debug_tile", "debug_timeout", "Sage2Error", "load_library",
            "attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "quant_flags", "QUANT_NO_SMOOTH_Q",
-           "QUANT_NO_SMOOTH_K", "QUANT_PER_BLOCK", "QUANT_SAGE1"]
+           "QUANT_NO_SMOOTH_K", "QUANT_PER_BLOCK", "QUANT_SAGE1", "attn_fwd_host",
+           "host_scratch_size", "host_status"]
 
 _DT = {torch.float16: FP16, torch.bfloat16: BF16, torch.float32: FP32}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # SAGE2_NOALLOC_SCRATCH_BYTES in include/sage2_attn.h
@@ -259,6 +260,51 @@ def debug_timeout(workspace, B, Hq, Hkv, Nq, Nkv, D, stream=None):
     _lib.check(_lib.lib().sage2_debug_timeout(B, Hq, Hkv, Nq, Nkv, D, _ptr(workspace),
                                               workspace.numel(), _stream(stream)),
                "sage2_debug_timeout")
+
+
+def host_scratch_size(B, Hq, Hkv, Nq, Nkv, D, out_dtype, kv_heads_per_chunk, quant_flags=0):
+    n = _lib.lib().sage2_host_scratch_size(B, Hq, Hkv, Nq, Nkv, D, _code(out_dtype),
+                                           int(kv_heads_per_chunk), int(quant_flags))
+    if n == 0:
+        raise Sage2Error(_lib.EINVAL, "sage2_host_scratch_size")
+    return int(n)
+
+
+def attn_fwd_host(q, k, v, out, causal=False, sm_scale=0.0, quant_flags=0, kv_heads_per_chunk=1,
+                  scratch=None, stream=None):
+    """The forward from host memory: q [B, Nq, Hq, D], k/v [B, Nkv, Hkv, D] and out
+    [B, Nq, Hq, D] are CPU tensors (pinned for the transfers to overlap the computation);
+    `scratch` a CUDA uint8 tensor of host_scratch_size(...) bytes (allocated if None). Runs in
+    chunks of kv_heads_per_chunk kv heads with copies in, computation and copies out overlapped;
+    the result equals attn_fwd on the whole problem. Returns the scratch tensor (for
+    host_status)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    B, Nq, Hq, D = q.shape
+    _, Nkv, Hkv, _ = k.shape
+    if k.shape != v.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes/dtypes disagree")
+    if tuple(out.shape) != (B, Nq, Hq, D):
+        raise ValueError("out shape")
+    n = host_scratch_size(B, Hq, Hkv, Nq, Nkv, D, out.dtype, kv_heads_per_chunk, quant_flags)
+    if scratch is None:
+        scratch = alloc_workspace(n)
+    _dev(scratch, "scratch")
+    _lib.check(_lib.lib().sage2_attn_fwd_host(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()), _code(q.dtype),
+        _code(out.dtype), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), float(sm_scale),
+        int(quant_flags), int(kv_heads_per_chunk), _ptr(scratch), scratch.numel(),
+        _stream(stream)), "sage2_attn_fwd_host")
+    return scratch
+
+
+def host_status(scratch, stream=None) -> tuple[int, int]:
+    """(status code, raw word) of the chunks of the last attn_fwd_host call on `scratch`."""
+    raw = ctypes.c_int(0)
+    rc = _lib.lib().sage2_host_status(_ptr(scratch), _stream(stream), ctypes.byref(raw))
+    return int(rc), int(raw.value)
 
 
 def attn_fwd_noalloc(q, k, v, out, causal=False, sm_scale=0.0, stream=None):

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsage2_attn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["sage2_api.cu", "sage2_prepass.cu", "sage2_attention.cu", "sage2_noalloc.cu"]
+SOURCES = ["sage2_api.cu", "sage2_prepass.cu", "sage2_attention.cu", "sage2_noalloc.cu",
+           "sage2_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -64,6 +64,9 @@ def _declare(lib):
                                 i),
         "sage2_debug_timeout": ([i, i, i, i, i, i, P, sz, P], i),
         "sage2_attn_fwd_noalloc": ([P, P, P, P, i, i, i, i, i, i, i, i, i, f, P], i),
+        "sage2_host_scratch_size": ([i] * 9, sz),
+        "sage2_attn_fwd_host": ([P, P, P, P, i, i, i, i, i, i, i, i, i, f, i, i, P, sz, P], i),
+        "sage2_host_status": ([P, P, ctypes.POINTER(i)], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

@@ -148,12 +148,12 @@ static int check_ws(const void *ws, size_t bytes, const Layout &L) {
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGE2_OK : SAGE2_ECUDA; }
 
-// The one path behind the dense and varlen prepass entry points.
-static int prepass_impl(const void *q, const void *k, const void *v, int in_dtype,
-                        const int *cu_q, const int *cu_kv, int B, int Hq, int Hkv, int max_nq,
-                        int max_nkv, int total_q, int total_kv, int D, int causal,
-                        float sm_scale, int quant_flags, void *ws, size_t ws_bytes,
-                        void *stream) {
+// The one path behind the dense and varlen prepass entry points (also used by the
+// host-streaming forward).
+int prepass_impl(const void *q, const void *k, const void *v, int in_dtype, const int *cu_q,
+                 const int *cu_kv, int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q,
+                 int total_kv, int D, int causal, float sm_scale, int quant_flags, void *ws,
+                 size_t ws_bytes, void *stream) {
   int rc = check_shapes(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
   if (in_dtype != SAGE2_FP16 && in_dtype != SAGE2_BF16) return SAGE2_EINVAL;
@@ -172,10 +172,10 @@ static int prepass_impl(const void *q, const void *k, const void *v, int in_dtyp
       launch_prepass(q, k, v, in_dtype, quant_flags, g, L, ws, (cudaStream_t)stream));
 }
 
-static int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q,
-                          const int *cu_kv, int B, int Hq, int Hkv, int max_nq, int max_nkv,
-                          int total_q, int total_kv, int D, int causal, float sm_scale,
-                          const void *ws, size_t ws_bytes, void *stream) {
+int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, const int *cu_kv,
+                   int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q, int total_kv,
+                   int D, int causal, float sm_scale, const void *ws, size_t ws_bytes,
+                   void *stream) {
   int rc = check_shapes(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
   if (!valid_quant_flags(quant_flags)) return SAGE2_EINVAL;

@@ -97,6 +97,18 @@ __host__ __device__ inline int kv_tiles_for(int qt, int nq, int nkv, int causal)
   return t < nt ? t : nt;
 }
 
+// ---------------------------------------------------------------- checked entry points
+// The prepass and attention calls behind the C ABI (argument checks, then the launches);
+// cu_q / cu_kv nullptr for dense problems. Return sage2_status codes.
+int prepass_impl(const void *q, const void *k, const void *v, int in_dtype, const int *cu_q,
+                 const int *cu_kv, int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q,
+                 int total_kv, int D, int causal, float sm_scale, int quant_flags, void *ws,
+                 size_t ws_bytes, void *stream);
+int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, const int *cu_kv,
+                   int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q, int total_kv,
+                   int D, int causal, float sm_scale, const void *ws, size_t ws_bytes,
+                   void *stream);
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
                            int quant_flags, const Geometry &g, const Layout &L, void *ws,

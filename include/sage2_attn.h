@@ -163,6 +163,26 @@ int sage2_attention_varlen_ex(void *out, int out_dtype, const int *cu_seqlens_q,
  * otherwise a code naming the wait that gave up). */
 int sage2_device_status(const void *workspace, void *stream, int *raw);
 
+/* The forward from host memory: q, k, v [B, Nq or Nkv, H, D] and out [B, Nq, Hq, D] are host
+ * pointers (page-locked for the copies to overlap; pageable memory works but serializes), the
+ * rest as sage2_attn_fwd, plus quant_flags (sage2_quant_flags, 0 for the method). The problem is
+ * run in chunks of kv_heads_per_chunk kv heads (and their q heads; it must divide Hkv): the
+ * copies in of one chunk and out of another overlap the computation of a third, on two copy
+ * streams of the library's own and the given stream. Results are those of sage2_attn_fwd on the
+ * whole problem. `scratch` is caller-owned device memory of at least sage2_host_scratch_size(...)
+ * bytes (two chunk slots: inputs, output, workspace); calls that overlap in time must not share
+ * it. The given stream completes after the last copy out. Device-side errors (bounded waits,
+ * format) are kept for sage2_host_status. Returns SAGE2_EINVAL / SAGE2_EWORKSPACE / SAGE2_ECUDA
+ * before or while queuing. */
+size_t sage2_host_scratch_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int out_dtype,
+                               int kv_heads_per_chunk, int quant_flags);
+int sage2_attn_fwd_host(const void *q, const void *k, const void *v, void *out, int in_dtype,
+                        int out_dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal,
+                        float sm_scale, int quant_flags, int kv_heads_per_chunk, void *scratch,
+                        size_t scratch_bytes, void *stream);
+/* As sage2_device_status, for the chunks of the last sage2_attn_fwd_host call on `scratch`. */
+int sage2_host_status(const void *scratch, void *stream, int *raw);
+
 /* Byte offsets of the buffers inside a workspace, for tests and tools that read the
  * intermediate results. Layouts (Tq, Tkv = padded token counts; every sequence starts on a
  * 128-row boundary at row 128 * (cu_seqlens[b] / 128 + b)):
