@@ -428,6 +428,30 @@ def test_int8_quantizer_invariants(oracle_mod):
             assert np.abs(qb - qc[grp, h] * float(sq[grp, h][0])).max() <= 0.5 * float(sq[grp, h][0]) * (1 + 1e-5)
 
 
+def test_k_channel_shift_leaves_softmax_rows_unchanged(oracle_mod):
+    """Adding the same vector c to every key of a (sequence, kv head) adds q . c to every logit
+    of a row, which softmax ignores: exact attention is unchanged up to FP64 rounding. With K
+    smoothing the quantized pipeline subtracts the shifted mean again, so on inputs whose means
+    are exact (keys in +-pairs) and an exactly representable shift its output is bit-identical;
+    without K smoothing the shift reaches the INT4 codes and changes it."""
+    q, k, v = _zero_error_inputs(11, with_means=False)
+    shift = np.zeros(k.shape[1])
+    shift[[3, 17, 62]] = [4.0, 2.5, 16.0]  # channel 62 is one Q uses (its 7s); 16 > every |K~|
+    assert np.abs(q[:, 62]).min() > 0
+    T = lambda a: torch.tensor(a)[:, None, :].half()
+    for causal in (False, True):
+        base = (bits(T(q)), bits(T(k)), bits(T(v)), F16, [0, len(q)], [0, len(k)], 1, 1, 64, causal)
+        moved = (bits(T(q)), bits(T(k + shift)), bits(T(v)), F16, [0, len(q)], [0, len(k)], 1, 1,
+                 64, causal)
+        np.testing.assert_allclose(oracle_mod.attention_exact(*moved),
+                                   oracle_mod.attention_exact(*base), rtol=1e-12, atol=1e-9)
+        np.testing.assert_array_equal(oracle_mod.attention_emulated(*moved, bq=8, bkv=16),
+                                      oracle_mod.attention_emulated(*base, bq=8, bkv=16))
+        a = oracle_mod.attention_emulated(*moved, bq=8, bkv=16, smooth_k=False)
+        b = oracle_mod.attention_emulated(*base, bq=8, bkv=16, smooth_k=False)
+        assert not np.array_equal(a, b)
+
+
 ABLATION_FLAGS = [dict(), dict(smooth_q=False), dict(smooth_k=False), dict(per_block=True),
                   dict(smooth_q=False, smooth_k=False, per_block=True),
                   dict(qk_bits=8, per_block=True, smooth_q=False), dict(qk_bits=8)]
