@@ -5,9 +5,11 @@
 // exactly into groups of kv heads (every quantity the method computes -- K channel means, V
 // scales, Q block means, DeltaS, the attention rows -- stays inside one kv head and its group
 // of q heads), so sage2_attn_fwd_host runs it group chunk by group chunk: while chunk c is
-// computed on the caller's stream, the inputs of chunk c + 1 are copied in on a copy stream and
-// the output of chunk c - 1 is copied out on another. Two device slots (inputs, output,
-// workspace) alternate. Chunk results are those of the whole problem, bit for bit.
+// computed, the inputs of chunk c + 1 are copied in on a copy stream and the output of chunk
+// c - 1 is copied out on another. Even chunks compute on the caller's stream and odd ones on a
+// second compute stream, so the first CTAs of one chunk fill the SMs that the last CTAs of the
+// previous one leave idle. Two device slots (inputs, output, workspace) alternate with the
+// chunks. Chunk results are those of the whole problem, bit for bit.
 #include <mutex>
 
 #include "sage2_device.cuh"
@@ -53,7 +55,7 @@ uint8_t *base1k(void *p) {
 struct DevPipe {
   std::mutex mu;
   bool ready = false;
-  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;  // comp: the odd chunks
   cudaEvent_t entry = nullptr, in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
 };
 constexpr int kMaxDevices = 64;
@@ -72,6 +74,7 @@ int init_pipe(DevPipe &p) {  // with p.mu held
   const unsigned ef = cudaEventDisableTiming;
   if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&p.entry, ef) != cudaSuccess)
     return SAGE2_ECUDA;
   for (int i = 0; i < 2; ++i)
@@ -144,8 +147,10 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
   SAGE2_CK(cudaEventRecord(pipe->entry, s0));  // copies start after the caller's earlier work
   SAGE2_CK(cudaStreamWaitEvent(pipe->h2d, pipe->entry, 0));
   SAGE2_CK(cudaStreamWaitEvent(pipe->d2h, pipe->entry, 0));
+  SAGE2_CK(cudaStreamWaitEvent(pipe->comp, pipe->entry, 0));
   for (int c = 0; c < p.chunks; ++c) {
     const int sl = c & 1;
+    const cudaStream_t cs = sl ? pipe->comp : s0;  // the slot's compute stream
     uint8_t *slot = base + 1024 + sl * p.slot;
     uint8_t *dq = slot, *dk = slot + p.q, *dv = dk + p.kv, *dout = dv + p.kv, *dws = dout + p.o;
     // inputs of chunk c (the slot's previous chunk, c - 2, has been computed)
@@ -159,18 +164,18 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
                                  rows_kv, cudaMemcpyHostToDevice, pipe->h2d));
     }
     SAGE2_CK(cudaEventRecord(pipe->in_done[sl], pipe->h2d));
-    // compute chunk c on the caller's stream (its output slot has been copied out)
-    SAGE2_CK(cudaStreamWaitEvent(s0, pipe->in_done[sl], 0));
-    if (c >= 2) SAGE2_CK(cudaStreamWaitEvent(s0, pipe->out_done[sl], 0));
+    // compute chunk c (its output slot has been copied out)
+    SAGE2_CK(cudaStreamWaitEvent(cs, pipe->in_done[sl], 0));
+    if (c >= 2) SAGE2_CK(cudaStreamWaitEvent(cs, pipe->out_done[sl], 0));
     rc = prepass_impl(dq, dk, dv, in_dtype, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq, Nkv, B * Nq,
-                      B * Nkv, D, causal, sm_scale, quant_flags, dws, p.ws, s0);
+                      B * Nkv, D, causal, sm_scale, quant_flags, dws, p.ws, cs);
     if (rc) return rc;
     rc = attention_impl(dout, out_dtype, quant_flags, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq,
-                        Nkv, B * Nq, B * Nkv, D, causal, sm_scale, dws, p.ws, s0);
+                        Nkv, B * Nq, B * Nkv, D, causal, sm_scale, dws, p.ws, cs);
     if (rc) return rc;
-    merge_status<<<1, 1, 0, s0>>>(reinterpret_cast<const int *>(base1k(dws)), status_total);
+    merge_status<<<1, 1, 0, cs>>>(reinterpret_cast<const int *>(base1k(dws)), status_total);
     SAGE2_CK(cudaGetLastError());
-    SAGE2_CK(cudaEventRecord(pipe->comp_done[sl], s0));
+    SAGE2_CK(cudaEventRecord(pipe->comp_done[sl], cs));
     // output of chunk c
     SAGE2_CK(cudaStreamWaitEvent(pipe->d2h, pipe->comp_done[sl], 0));
     SAGE2_CK(cudaMemcpy2DAsync(static_cast<uint8_t *>(out) + c * ow, opitch, dout, ow, ow, rows_q,
