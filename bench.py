@@ -123,7 +123,10 @@ def aggregate_value(ops_per_rank: float, seconds_max: float, world: int) -> floa
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples every 50 ms; start() returns once the first sample is
+    in, and stop(t0, t1) keeps the samples taken inside the timed window [t0, t1] (host clock),
+    or the nearest ones when the window is shorter than the sampling period (said so)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -138,14 +141,31 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        t_end = time.time() + 5.0
+        while time.time() < t_end and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
-    def stop(self) -> dict:
+    @staticmethod
+    def _ts(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, t0=None, t1=None) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)  # one more period, so that a sample follows the window's end
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -154,19 +174,31 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
+            if len(parts) >= 10:
                 rows.append(parts)
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        window = "all samples"
+        if t0 is not None and t1 is not None:
+            stamped = [(self._ts(r[0]), r) for r in rows]
+            inside = [r for ts, r in stamped if ts is not None and t0 <= ts <= t1]
+            if inside:
+                rows, window = inside, "inside the timed region"
+            else:
+                near = sorted((abs(ts - 0.5 * (t0 + t1)), i) for i, (ts, r) in enumerate(stamped)
+                              if ts is not None)[:2]
+                if near:
+                    rows = [stamped[i][1] for _, i in near]
+                    window = "nearest to the timed region (shorter than the sampling period)"
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
         loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "window": window}
 
 
 def measured_peaks():
@@ -260,6 +292,7 @@ def run_ours(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
+    t_region0 = time.time()
     for i in range(args.steps):
         flush.zero_()  # evict L2 between steps (outside the timed events)
         ev[i][0].record(stream)
@@ -268,9 +301,10 @@ def run_ours(args, rank, world, local):
         attention()
         ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
+    t_region1 = time.time()
     barrier(world)
     t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
+    clk = clocks.stop(t_region0, t_region1)
     rc, raw = S.device_status(ws, stream)
     if rc != 0:
         raise RuntimeError(f"device status after the timed steps: {rc} {raw:#x}")
@@ -392,7 +426,7 @@ def run_reference(args, rank, world):
         return
     w = WORKLOADS[args.workload]
     x = W.make_inputs(w)
-    units, sops = oracle_sample(w, x, max(2, sample_size(w) // 4))
+    units, sops = oracle_sample(w, x, sample_size(w))  # the cpu_baseline sample
     for _ in range(args.warmup):  # untimed, on a single unit to keep the run short
         run_oracle_sample(w, x, units[:1], args.quant)
     times, cores = [], 1
