@@ -98,3 +98,53 @@ def test_varlen_requires_cu_seqlens(lib):
     rc = lib.sage2_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, 1, 1, FAKE, FAKE, 2, 4, 2, 10, 64,
                                    100, 100, 128, 0, 0.0, FAKE, 1 << 40, None)
     assert rc == _lib.EINVAL
+
+
+def test_workspace_size_per_code_format(lib):
+    """The INT8 (v1) path stores two-byte Q and K codes: its workspace is larger by exactly the
+    extra code bytes (rounded to the 1 KB granule); invalid switch words give 0."""
+    args = (1, 8, 2, 1000, 1500, 128, 1000, 1500)
+    n4 = lib.sage2_workspace_size(*args)
+    assert n4 > 0 and lib.sage2_workspace_size_ex(*args, 0) == n4
+    assert lib.sage2_workspace_size_ex(*args, 1 | 2 | 4) == n4  # ablations: same layout
+    n8 = lib.sage2_workspace_size_ex(*args, 8)
+    L4, L8 = _lib.WsLayout(), _lib.WsLayout()
+    assert lib.sage2_workspace_layout_ex(*args, 0, ctypes.byref(L4)) == 0
+    assert lib.sage2_workspace_layout_ex(*args, 8, ctypes.byref(L8)) == 0
+    assert (L4.code_bytes, L8.code_bytes) == (1, 2)
+    extra = (L8.kcode - L8.qcode) - (L4.kcode - L4.qcode)  # the Q code region doubled
+    assert extra >= 8 * L4.Tq * 128 - 1024
+    assert n8 > n4
+    for bad in (16, 8 | 4, -1):
+        assert lib.sage2_workspace_size_ex(*args, bad) == 0
+        assert lib.sage2_workspace_layout_ex(*args, bad, ctypes.byref(L8)) == _lib.EINVAL
+
+
+def test_ex_entry_points_reject_bad_switches_before_cuda(lib):
+    cu = FAKE
+    rc = lib.sage2_prepass_varlen_ex(FAKE, FAKE, FAKE, 1, cu, cu, 1, 2, 2, 128, 128, 128, 128, 64,
+                                     0, 0.0, 8 | 1, FAKE, 1 << 30, None)
+    assert rc == _lib.EINVAL
+    rc = lib.sage2_attention_varlen_ex(FAKE, 2, cu, cu, 1, 2, 2, 128, 128, 128, 128, 64, 0, 0.0,
+                                       32, FAKE, 1 << 30, None)
+    assert rc == _lib.EINVAL
+
+
+def test_host_forward_scratch_size(lib):
+    """Two slots, each holding one chunk's inputs, output and workspace: more chunks need less
+    scratch; chunk sizes that do not divide Hkv (or bad types) give 0 / SAGE2_EINVAL."""
+    B, Hq, Hkv, N, D = 1, 32, 8, 4096, 128
+    sizes = [lib.sage2_host_scratch_size(B, Hq, Hkv, N, N, D, 1, c, 0) for c in (8, 4, 2, 1)]
+    assert all(s > 0 for s in sizes) and sizes == sorted(sizes, reverse=True)
+    one_chunk_inputs = B * N * (Hq + 2 * Hkv) * D * 2
+    assert sizes[0] >= 2 * one_chunk_inputs  # two slots of the whole problem
+    assert lib.sage2_host_scratch_size(B, Hq, Hkv, N, N, D, 1, 3, 0) == 0
+    assert lib.sage2_host_scratch_size(B, Hq, Hkv, N, N, D, 7, 1, 0) == 0
+    assert lib.sage2_host_scratch_size(B, Hq, Hkv, N, N, D, 1, 1, 8) > sizes[3]  # 2-byte codes
+    out = ctypes.c_void_p(0x20000)
+    rc = lib.sage2_attn_fwd_host(FAKE, FAKE, FAKE, out, 1, 1, B, Hq, Hkv, N, N, D, 0, 0.0, 0, 3,
+                                 FAKE, 1 << 40, None)
+    assert rc == _lib.EINVAL
+    rc = lib.sage2_attn_fwd_host(FAKE, FAKE, FAKE, out, 1, 1, B, Hq, Hkv, N, N, D, 0, 0.0, 0, 1,
+                                 FAKE, 16, None)
+    assert rc == _lib.EWORKSPACE
