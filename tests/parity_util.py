@@ -57,7 +57,7 @@ def e4m3_to_f64(u8: torch.Tensor) -> np.ndarray:
     return u8.contiguous().view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy()
 
 
-class GpuRun:
+class GpuCase:
     """Inputs on the GPU plus a workspace; prepass / attention / debug hooks."""
 
     def __init__(self, w: W.Workload, x: dict, causal=None, sm_scale=0.0, quant_flags=0):
@@ -196,7 +196,7 @@ def unit_rows(w: W.Workload, cu_q, units):
 
 
 # ---------------------------------------------------------------- checks shared by GPU tests
-def compare_p_codes(g: GpuRun, w: W.Workload, x: dict, kw: dict):
+def compare_p_codes(g: GpuCase, w: W.Workload, x: dict, kw: dict):
     """P~ e4m3 codes of a few tiles per sequence (first, middle, last Q tile; first, middle and
     last visited KV tile) from the kernel against the emulation's, for the oracle switches kw.
     Every disagreement must be one e4m3 step, at an exact 448 P within 4 ulp of the rounding

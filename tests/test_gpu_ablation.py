@@ -31,7 +31,7 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import (GpuRun, bits, c32_of, check_forward_with_flips, compare_p_codes, kv_tiles,
+from parity_util import (GpuCase, bits, c32_of, check_forward_with_flips, compare_p_codes, kv_tiles,
                          metrics, pad_starts)
 
 pytestmark = pytest.mark.gpu
@@ -81,7 +81,7 @@ def test_flag_word_and_invalid_bits():
     assert S.quant_flags() == 0
     assert S.quant_flags(smooth_q=False, smooth_k=False, per_block=True) == 7
     w, x = _case("prefill")
-    g = GpuRun(w, x)
+    g = GpuCase(w, x)
     for bad in (16, S.QUANT_SAGE1 | S.QUANT_PER_BLOCK):  # an unknown bit; SAGE1 combined
         g.quant_flags = bad
         with pytest.raises(S.Sage2Error):
@@ -93,7 +93,7 @@ def test_flag_word_and_invalid_bits():
 def test_prepass_bit_exact_with_switches(name, setting):
     kw = SETTINGS[setting]
     w, x = _case(name)
-    g = GpuRun(w, x, quant_flags=S.quant_flags(**kw))
+    g = GpuCase(w, x, quant_flags=S.quant_flags(**kw))
     g.prepass()
     assert g.status() == (0, 0)
     got = g.gathered()
@@ -131,7 +131,7 @@ def test_prepass_bit_exact_with_switches(name, setting):
 def test_p_codes_agree_except_at_exp2_rounding_midpoints(name, setting):
     kw = SETTINGS[setting]
     w, x = _case(name)
-    g = GpuRun(w, x, quant_flags=S.quant_flags(**kw))
+    g = GpuCase(w, x, quant_flags=S.quant_flags(**kw))
     g.prepass()
     n_diff, n_cmp = compare_p_codes(g, w, x, kw)
     assert n_diff <= 1e-3 * n_cmp, (n_diff, n_cmp)
@@ -147,7 +147,7 @@ def test_pv_tile_accumulator_is_fp32_class():
     worst = 0.0
     for name in ("prefill", "dit"):
         w, x = _case(name)
-        g = GpuRun(w, x)
+        g = GpuCase(w, x)
         g.prepass()
         dt = W.dtype_code(w)
         _, vamax = oracle.kv_stats(bits(x["k"]), bits(x["v"]), dt, x["cu_kv"], w.hkv, w.d)
@@ -179,7 +179,7 @@ def test_pv_tile_accumulator_is_fp32_class():
 def test_forward_matches_emulation_with_switches(name, setting):
     kw = SETTINGS[setting]
     w, x = _case(name)
-    g = GpuRun(w, x, quant_flags=S.quant_flags(**kw))
+    g = GpuCase(w, x, quant_flags=S.quant_flags(**kw))
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle.attention_emulated(*_args(w, x), **kw)
@@ -190,7 +190,7 @@ def test_dense_entry_with_switches_equals_varlen():
     w = W.scaled(W.PREFILL, (384, 384), (384, 384), hq=4, hkv=2, name="dense_eq")
     x = W.make_inputs(w)
     f = S.quant_flags(smooth_q=False, per_block=True)
-    a = GpuRun(w, x, quant_flags=f).forward(out_dtype=torch.float32)
+    a = GpuCase(w, x, quant_flags=f).forward(out_dtype=torch.float32)
     q = x["q"].view(2, 384, 4, 128).cuda()
     k = x["k"].view(2, 384, 2, 128).cuda()
     v = x["v"].view(2, 384, 2, 128).cuda()
@@ -204,7 +204,7 @@ def _errors(name):
     ex = oracle.attention_exact(*_args(w, x))
     res = {}
     for setting, kw in SETTINGS.items():
-        g = GpuRun(w, x, quant_flags=S.quant_flags(**kw))
+        g = GpuCase(w, x, quant_flags=S.quant_flags(**kw))
         out = g.forward(out_dtype=torch.float32).cpu().numpy()
         emu = oracle.attention_emulated(*_args(w, x), **kw)
         res[setting] = (metrics(out, ex), metrics(emu, ex))

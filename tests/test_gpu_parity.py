@@ -17,7 +17,7 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import (GpuRun, bits, c32_of, e4m3_to_f64, kv_tiles, metrics, pad_starts,
+from parity_util import (GpuCase, bits, c32_of, e4m3_to_f64, kv_tiles, metrics, pad_starts,
                          unit_rows, units_sample)
 
 pytestmark = pytest.mark.gpu
@@ -60,7 +60,7 @@ def run_case(name):
     if name not in _cache:
         w = SCALED[name]
         x = W.make_inputs(w)
-        g = GpuRun(w, x)
+        g = GpuCase(w, x)
         _cache[name] = (w, x, g)
     return _cache[name]
 
@@ -185,7 +185,7 @@ def test_dense_entry_point_equals_varlen():
     # prefill_s has two sequences of different length: use a uniform one for the dense call
     w2 = W.scaled(W.PREFILL, (384, 384), (384, 384), hq=4, hkv=2, name="dense_eq")
     x2 = W.make_inputs(w2)
-    g2 = GpuRun(w2, x2)
+    g2 = GpuCase(w2, x2)
     a = g2.forward(out_dtype=torch.float32)
     q = x2["q"].view(2, 384, 4, 128).cuda()
     k = x2["k"].view(2, 384, 2, 128).cuda()
@@ -221,7 +221,7 @@ def test_edge_cases(case):
     nq, nkv, hq, hkv, d, causal, dt = case
     w = W.Workload("edge", nq, nkv, hq, hkv, d, dt, causal, "kbias9", 31, varlen=True)
     x = W.make_inputs(w)
-    g = GpuRun(w, x)
+    g = GpuCase(w, x)
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle_ref(w, x)
@@ -240,7 +240,7 @@ def test_edge_cases(case):
 def test_sm_scale_argument():
     w = W.scaled(W.TINY, (200,), (300,), hq=2, hkv=2)
     x = W.make_inputs(w)
-    g = GpuRun(w, x, sm_scale=0.05)
+    g = GpuCase(w, x, sm_scale=0.05)
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     emu = oracle.attention_emulated(bits(x["q"]), bits(x["k"]), bits(x["v"]), 0, x["cu_q"],
                                     x["cu_kv"], 2, 2, 64, False, 0.05)
@@ -256,7 +256,7 @@ def test_full_size_sampled_units(wl):
     >= 32 seeded (sequence, head, Q block) units including every last partial block, the
     first block and a causal-diagonal block."""
     x = W.make_inputs(wl)
-    g = GpuRun(wl, x)
+    g = GpuCase(wl, x)
     out = g.forward(out_dtype=torch.float32)
     assert g.status() == (0, 0)
     units = units_sample(wl, 32, seed=wl.seed)
@@ -272,7 +272,7 @@ def test_full_size_full_output(wl):
     """The LLM prefill and varlen workloads at full size, every output element against the
     oracle's emulation (the oracle runs the whole workload on the host cores)."""
     x = W.make_inputs(wl)
-    g = GpuRun(wl, x)
+    g = GpuCase(wl, x)
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle_ref(wl, x)
@@ -296,7 +296,7 @@ def test_full_size_full_output(wl):
 def test_bounded_wait_reports_timeout_and_context_survives():
     w = W.TINY
     x = W.make_inputs(w)
-    g = GpuRun(w, x)
+    g = GpuCase(w, x)
     g.prepass()
     S.debug_timeout(g.ws, 1, 2, 2, 256, 256, 64)
     code, raw = g.status()

@@ -21,7 +21,7 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import (GpuRun, bits, check_forward_with_flips, compare_p_codes, kv_tiles,
+from parity_util import (GpuCase, bits, check_forward_with_flips, compare_p_codes, kv_tiles,
                          metrics, unit_rows, units_sample)
 
 pytestmark = pytest.mark.gpu
@@ -64,7 +64,7 @@ def _args(w, x):
 @pytest.mark.parametrize("name", ["tiny", "prefill", "dit", "varlen"])
 def test_prepass_bit_exact(name):
     w, x = _case(name)
-    g = GpuRun(w, x, quant_flags=F)
+    g = GpuCase(w, x, quant_flags=F)
     assert g.L.code_bytes == 2
     g.prepass()
     assert g.status() == (0, 0)
@@ -89,7 +89,7 @@ def test_prepass_bit_exact(name):
 @pytest.mark.parametrize("name", ["tiny", "prefill", "dit", "varlen"])
 def test_qk_accumulators_bit_exact(name):
     w, x = _case(name)
-    g = GpuRun(w, x, quant_flags=F)
+    g = GpuCase(w, x, quant_flags=F)
     g.prepass()
     dt = W.dtype_code(w)
     kmean, _ = oracle.kv_stats(bits(x["k"]), bits(x["v"]), dt, x["cu_kv"], w.hkv, w.d)
@@ -127,7 +127,7 @@ def test_qk_accumulators_bit_exact(name):
 @pytest.mark.parametrize("name", ["prefill", "dit", "varlen"])
 def test_p_codes_agree_except_at_exp2_rounding_midpoints(name):
     w, x = _case(name)
-    g = GpuRun(w, x, quant_flags=F)
+    g = GpuCase(w, x, quant_flags=F)
     g.prepass()
     n_diff, n_cmp = compare_p_codes(g, w, x, KW)
     assert n_diff <= 1e-3 * n_cmp, (n_diff, n_cmp)
@@ -136,7 +136,7 @@ def test_p_codes_agree_except_at_exp2_rounding_midpoints(name):
 @pytest.mark.parametrize("name", list(CASES))
 def test_forward_matches_emulation(name):
     w, x = _case(name)
-    g = GpuRun(w, x, quant_flags=F)
+    g = GpuCase(w, x, quant_flags=F)
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     check_forward_with_flips(out, oracle.attention_emulated(*_args(w, x), **KW), x)
@@ -148,8 +148,8 @@ def test_int8_path_is_more_accurate_than_int4(name):
     these distributions, and errs less than the INT4 method (as in the emulation)."""
     w, x = _case(name)
     ex = oracle.attention_exact(*_args(w, x))
-    o1 = GpuRun(w, x, quant_flags=F).forward(out_dtype=torch.float32).cpu().numpy()
-    o2 = GpuRun(w, x).forward(out_dtype=torch.float32).cpu().numpy()
+    o1 = GpuCase(w, x, quant_flags=F).forward(out_dtype=torch.float32).cpu().numpy()
+    o2 = GpuCase(w, x).forward(out_dtype=torch.float32).cpu().numpy()
     m1, m2 = metrics(o1, ex), metrics(o2, ex)
     assert m1["cos"] >= 0.99 and m1["relL1"] <= 0.06, m1
     assert m1["relL1"] < m2["relL1"], (m1, m2)
@@ -171,7 +171,7 @@ def test_edge_cases(case):
     nq, nkv, hq, hkv, d, causal, dt = case
     w = W.Workload("edge", nq, nkv, hq, hkv, d, dt, causal, "kbias9", 31, varlen=True)
     x = W.make_inputs(w)
-    g = GpuRun(w, x, quant_flags=F)
+    g = GpuCase(w, x, quant_flags=F)
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle.attention_emulated(*_args(w, x), **KW)
@@ -188,7 +188,7 @@ def test_edge_cases(case):
 def test_dense_entry_equals_varlen():
     w = W.scaled(W.PREFILL, (384, 384), (384, 384), hq=4, hkv=2, name="dense_eq")
     x = W.make_inputs(w)
-    a = GpuRun(w, x, quant_flags=F).forward(out_dtype=torch.float32)
+    a = GpuCase(w, x, quant_flags=F).forward(out_dtype=torch.float32)
     q = x["q"].view(2, 384, 4, 128).cuda()
     k = x["k"].view(2, 384, 2, 128).cuda()
     v = x["v"].view(2, 384, 2, 128).cuda()
@@ -201,7 +201,7 @@ def test_format_mismatch_is_refused_on_the_device():
     nothing and reports SAGE2_EINVAL through the device status; the context stays usable."""
     w, x = _case("tiny")
     # INT8 workspace, INT4 kernel: the workspace is large enough for either
-    g = GpuRun(w, x, quant_flags=F)
+    g = GpuCase(w, x, quant_flags=F)
     g.prepass()
     out = torch.full((g.tq, w.hq, w.d), 7.0, dtype=torch.float32, device="cuda")
     S.attention_varlen(out, g.ws, g.cu_q, g.cu_kv, w.hkv, g.max_nq, g.max_nkv, g.tkv,
@@ -210,7 +210,7 @@ def test_format_mismatch_is_refused_on_the_device():
     assert code == -1 and raw == 0x300, (code, hex(raw))
     assert torch.all(out == 7.0)
     # INT4 workspace, INT8 kernel
-    g2 = GpuRun(w, x)
+    g2 = GpuCase(w, x)
     g2.prepass()
     ws_big = torch.zeros(S.workspace_size(w.batch, w.hq, w.hkv, g2.max_nq, g2.max_nkv, w.d,
                                           g2.tq, g2.tkv, quant_flags=F), dtype=torch.uint8,
@@ -224,7 +224,7 @@ def test_format_mismatch_is_refused_on_the_device():
     assert code == -1 and raw == 0x300, (code, hex(raw))
     assert torch.all(out == 7.0)
     # and a correct call afterwards works
-    ok = GpuRun(w, x, quant_flags=F).forward(out_dtype=torch.float32).cpu().numpy()
+    ok = GpuCase(w, x, quant_flags=F).forward(out_dtype=torch.float32).cpu().numpy()
     assert metrics(ok, oracle.attention_emulated(*_args(w, x), **KW))["relL1"] <= 1e-3
 
 
@@ -234,7 +234,7 @@ def test_full_size_sampled_units(wl):
     computes >= 32 seeded (sequence, head, Q block) units including the last partial block,
     the first block and a causal-diagonal block."""
     x = W.make_inputs(wl)
-    g = GpuRun(wl, x, quant_flags=F)
+    g = GpuCase(wl, x, quant_flags=F)
     out = g.forward(out_dtype=torch.float32)
     assert g.status() == (0, 0)
     units = units_sample(wl, 32, seed=wl.seed)
