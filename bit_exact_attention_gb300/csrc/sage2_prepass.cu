@@ -86,11 +86,16 @@ __device__ __forceinline__ void flag_bad_seq(int *status) {
 }
 
 // ------------------------------------------------------------------ 1a. K/V statistics
-// grid (nchunk, B, ceil(Hkv * D0 / 8 / kStatThreads)), block kStatThreads. Each thread owns a
-// run of 8 channels (one 16-byte vector of a token row) and walks kStatChunk tokens.
+// grid (nchunk, B, ceil(nvec / VPB)), block kStatThreads, nvec = Hkv * D0 / 8 vectors of 8
+// channels per token. A block covers VPB = min(nvec, kStatThreads) vectors and splits the
+// chunk's kStatChunk tokens over L = kStatThreads / VPB token lanes (a row of few vectors, as in
+// a chunk of one kv head, still keeps the block busy); each thread walks its tokens with
+// double-float sums, and the lanes' partials (each exact) are added in lane order in FP64.
 constexpr int kStatThreads = 128;
 template <bool BF16>
 __global__ void __launch_bounds__(kStatThreads) kv_stats_partial(PrepassArgs a) {
+  __shared__ double lane_sum[kStatThreads][8];
+  __shared__ float lane_max[kStatThreads][8];
   const int b = blockIdx.y, chunk = blockIdx.x;
   const Geometry &g = a.g;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
@@ -103,27 +108,30 @@ __global__ void __launch_bounds__(kStatThreads) kv_stats_partial(PrepassArgs a) 
   const int t1 = min(t0 + kStatChunk, s.nkv);
   const int row_elems = g.Hkv * g.D0;
   const int nvec = row_elems / 8;
-  {
-    const int vi = blockIdx.z * kStatThreads + threadIdx.x;
-    if (vi >= nvec) return;
-    float hi[8], lo[8], mx[8];
+  const int vpb = min(nvec, kStatThreads), lanes = kStatThreads / vpb;
+  const int vl = threadIdx.x % vpb, lane = threadIdx.x / vpb;
+  const int vi = blockIdx.z * vpb + vl;
+  const bool active = lane < lanes && vi < nvec;
+  float hi[8], lo[8], mx[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) hi[e] = lo[e] = mx[e] = 0.f;
+  for (int e = 0; e < 8; ++e) hi[e] = lo[e] = mx[e] = 0.f;
+  if (active) {
     const uint4 *kp = reinterpret_cast<const uint4 *>(a.k + (size_t)(s.kv0 + t0) * row_elems) + vi;
     const uint4 *vp = reinterpret_cast<const uint4 *>(a.v + (size_t)(s.kv0 + t0) * row_elems) + vi;
     const int stride = nvec;
     constexpr int U = 8;  // tokens whose loads are all issued before any is used
 #pragma unroll 1
-    for (int t = t0; t < t1; t += U) {
+    for (int t = t0 + lane; t < t1; t += U * lanes) {
       uint4 kk[U], vv[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {  // tokens past the end read as 0 and add nothing
-        const bool ok = t + u < t1;
-        kk[u] = ok ? __ldg(kp + (size_t)(t - t0 + u) * stride) : make_uint4(0u, 0u, 0u, 0u);
-        vv[u] = ok ? __ldg(vp + (size_t)(t - t0 + u) * stride) : make_uint4(0u, 0u, 0u, 0u);
+        const int tu = t + u * lanes;
+        const bool ok = tu < t1;
+        kk[u] = ok ? __ldg(kp + (size_t)(tu - t0) * stride) : make_uint4(0u, 0u, 0u, 0u);
+        vv[u] = ok ? __ldg(vp + (size_t)(tu - t0) * stride) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {  // tokens in order
+      for (int u = 0; u < U; ++u) {
         float xk[8], xv[8];
         unpack8<BF16>(kk[u], xk);
         unpack8<BF16>(vv[u], xv);
@@ -135,12 +143,38 @@ __global__ void __launch_bounds__(kStatThreads) kv_stats_partial(PrepassArgs a) 
         }
       }
     }
+  }
+  if (lanes > 1) {  // block-uniform: combine the token lanes of each vector
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      lane_sum[threadIdx.x][e] = (double)hi[e] + (double)lo[e];
+      lane_max[threadIdx.x][e] = mx[e];
+    }
+    __syncthreads();
+    if (lane != 0 || !active) return;
+    double sum[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[e] = lane_sum[vl][e];
+    for (int l = 1; l < lanes; ++l)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sum[e] += lane_sum[l * vpb + vl][e];
+        mx[e] = fmaxf(mx[e], lane_max[l * vpb + vl][e]);
+      }
     const size_t o = ((size_t)b * a.L.nchunk + chunk) * row_elems + (size_t)vi * 8;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      a.w.kpart[o + e] = (double)hi[e] + (double)lo[e];
+      a.w.kpart[o + e] = sum[e];
       a.w.vpart[o + e] = mx[e];
     }
+    return;
+  }
+  if (!active) return;
+  const size_t o = ((size_t)b * a.L.nchunk + chunk) * row_elems + (size_t)vi * 8;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    a.w.kpart[o + e] = (double)hi[e] + (double)lo[e];
+    a.w.vpart[o + e] = mx[e];
   }
 }
 
@@ -678,7 +712,8 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   // every grid dimension at least 1 (a zero-length maximum is legal; the kernels bound-check)
   const int kv_tiles = max(1, (g.max_nkv + kBKV - 1) / kBKV);
   const int q_tiles = max(1, (g.max_nq + kBQ - 1) / kBQ);
-  const dim3 stat_grid(L.nchunk, g.B, (nvec + kStatThreads - 1) / kStatThreads);
+  const int stat_vpb = min(nvec, kStatThreads);
+  const dim3 stat_grid(L.nchunk, g.B, (nvec + stat_vpb - 1) / stat_vpb);
   const dim3 kv_grid(kv_tiles, g.Hkv, g.B);
   const dim3 q_grid(q_tiles, g.Hq, g.B);
   // DeltaS row-tile height: the fewest computed rows for the (Q block, head) rows of a kv
