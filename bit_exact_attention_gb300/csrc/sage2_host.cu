@@ -139,9 +139,20 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
   const size_t qw = (size_t)p.hq_c * D * ib, kw = (size_t)p.hk_c * D * ib, ow = (size_t)p.hq_c * D * ob;
   const size_t qpitch = (size_t)Hq * D * ib, kpitch = (size_t)Hkv * D * ib, opitch = (size_t)Hq * D * ob;
 
-#define SAGE2_CK(x)                       \
-  do {                                    \
-    if ((x) != cudaSuccess) return SAGE2_ECUDA; \
+  // On an error after work was queued, the given stream still waits for everything queued on
+  // the copy and compute streams (a caller that synchronizes it may then reuse its buffers).
+  auto join = [&]() {
+    cudaEvent_t done[3] = {pipe->in_done[0], pipe->comp_done[0], pipe->out_done[0]};
+    const cudaStream_t side[3] = {pipe->h2d, pipe->comp, pipe->d2h};
+    for (int i = 0; i < 3; ++i)
+      if (cudaEventRecord(done[i], side[i]) == cudaSuccess) cudaStreamWaitEvent(s0, done[i], 0);
+  };
+#define SAGE2_CK(x)              \
+  do {                           \
+    if ((x) != cudaSuccess) {    \
+      join();                    \
+      return SAGE2_ECUDA;        \
+    }                            \
   } while (0)
   SAGE2_CK(cudaMemsetAsync(status_total, 0, sizeof(int), s0));
   SAGE2_CK(cudaEventRecord(pipe->entry, s0));  // copies start after the caller's earlier work
@@ -169,10 +180,13 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
     if (c >= 2) SAGE2_CK(cudaStreamWaitEvent(cs, pipe->out_done[sl], 0));
     rc = prepass_impl(dq, dk, dv, in_dtype, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq, Nkv, B * Nq,
                       B * Nkv, D, causal, sm_scale, quant_flags, dws, p.ws, cs);
-    if (rc) return rc;
-    rc = attention_impl(dout, out_dtype, quant_flags, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq,
-                        Nkv, B * Nq, B * Nkv, D, causal, sm_scale, dws, p.ws, cs);
-    if (rc) return rc;
+    if (rc == SAGE2_OK)
+      rc = attention_impl(dout, out_dtype, quant_flags, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq,
+                          Nkv, B * Nq, B * Nkv, D, causal, sm_scale, dws, p.ws, cs);
+    if (rc) {
+      join();
+      return rc;
+    }
     merge_status<<<1, 1, 0, cs>>>(reinterpret_cast<const int *>(base1k(dws)), status_total);
     SAGE2_CK(cudaGetLastError());
     SAGE2_CK(cudaEventRecord(pipe->comp_done[sl], cs));
