@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "sage2_device.cuh"
@@ -84,7 +85,7 @@ constexpr uint32_t kTmemCols = 512;
 enum : int {
   kSiteQ = 1, kSiteKvFull = 2, kSiteKvEmpty = 3, kSiteSFull = 4, kSitePFull = 5, kSiteRFull = 6,
   kSiteRFree = 7, kSiteKvFullSm = 8, kSiteAFull = 9, kSiteLFull = 10, kSiteSFree = 11,
-  kSitePvDone = 12
+  kSitePvDone = 12, kSiteTok = 13
 };
 
 struct AttnArgs {
@@ -584,6 +585,421 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- two-tile (ping-pong) kernel
+// One CTA per (sequence, q head, pair of 128-row Q tiles); the two tiles share every K/V stage,
+// so each K/V byte brought in feeds twice the tensor work. Warps: 0 TMA producer, 1 MMA issuer,
+// 2 idle, 3 stages the V channel scales, 4-7 softmax + epilogue of tile 0, 8-11 of tile 1 (each
+// SM sub-partition runs one softmax warp of each tile, so one tile's arithmetic fills the
+// other's MMA latency).
+// Per tile t: tensor memory S_t [256 t, 256 t + 128) and O_t [256 t + 128, 256 t + 128 + DP) (the
+// FP32 output accumulator); Q_t codes and P~_t (128 x 128 e4m3, the A operand of P~V) in shared
+// memory, 128-byte swizzled K-major. Per KV tile j the softmax loads S_t(j) into registers and
+// releases S_t at once (QK_t(j+1) may start), computes P~_t(j), waits for PV_t(j-1), rescales
+// O_t by alpha(j) (skipped when every row of the warp has alpha = 1), writes P~_t(j) and hands
+// it to the issuer; PV_t(j) then adds the block partial P~(j) V(j) into O_t.
+// The issuer is event driven: it issues whichever of QK_0, PV_0, QK_1, PV_1 is ready.
+// The softmax warps of the two tiles that share a sub-partition take turns on the logits phase
+// (ALU bound: dequantize, DeltaS, row max): tile 1 starts logits(j) once tile 0 has finished
+// logits(j), tile 0 starts logits(j+1) once tile 1 has finished logits(j). So one warp's
+// exponentials (MUFU bound) overlap the other's logits instead of both warps doing the same phase.
+template <int DP, int ST>
+struct PPPlan {
+  static constexpr int kQ = 0;                       // [2][128 rows][DP]   (swizzled)
+  static constexpr int kP = kQ + 2 * 128 * DP;       // [2][128 rows][128]  (128B swizzled)
+  static constexpr int kK = kP + 2 * 128 * 128;      // [ST][128 keys][DP]  (swizzled)
+  static constexpr int kV = kK + ST * 128 * DP;      // [ST][DP][128 keys]  (swizzled)
+  static constexpr int kDsc = kV + ST * DP * 128;    // float [ST][2][128]
+  static constexpr int kSk = kDsc + ST * 2 * 512;    // float [ST][4]
+  static constexpr int kSv = kSk + ST * 16;          // float [DP]
+  static constexpr int kBar = kSv + DP * 4;
+  // q, full[ST], empty[ST], s_full[2], s_free[2], p_full[2], pv_done[2], drain, tok[2][4]
+  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 2 + 2 + 1 + 8;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kEnd = kMisc + 16;
+  static constexpr int kBytes = kEnd + 1024;
+  static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
+};
+// register split: the control warpgroup keeps 56 (its event loop spills at 40), the two softmax
+// warpgroups take 224 each (56 + 2 x 224 = 3 x 168, the launch budget)
+constexpr int kPPRegsCtl = 56, kPPRegsSoftmax = 224;
+static_assert(kPPRegsCtl + 2 * kPPRegsSoftmax <= 3 * kRegsLaunch, "register split above budget");
+// tensor-memory columns of tile t: S at 256 t, O at 256 t + 128
+__device__ __forceinline__ uint32_t pp_col_s(int t) { return (uint32_t)t * 256u; }
+__device__ __forceinline__ uint32_t pp_col_o(int t) { return (uint32_t)t * 256u + 128u; }
+
+template <int DP, int ST>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_pp(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+  using P = PPPlan<DP, ST>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const Geometry &g = a.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int format = a.status[1];
+  const int b = blockIdx.z, hq = blockIdx.y;
+  const int pair = g.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
+  if (format != kFormatInt4) {
+    if (tid == 0) atomicCAS(a.status, 0, kStatusFormat);
+    return;
+  }
+  if (!s.ok || 2 * pair * kBQ >= s.nq) return;
+  const int hk = hq / (g.Hq / g.Hkv);
+  int qtt[2], Tt[2];
+  bool valid[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    qtt[t] = 2 * pair + t;
+    valid[t] = qtt[t] * kBQ < s.nq;
+    Tt[t] = valid[t] ? kv_tiles_for(qtt[t], s.nq, s.nkv, g.causal) : 0;
+  }
+  const int Tmax = max(Tt[0], Tt[1]);
+  if (Tmax == 0) {  // no visible key for any row of either tile: the output is 0
+    for (int t = 0; t < 2; ++t)
+      if (valid[t] && tid < kBQ && qtt[t] * kBQ + tid < s.nq) {
+        const size_t o = ((size_t)(s.q0 + qtt[t] * kBQ + tid) * g.Hq + hq) * g.D0;
+        for (int d = 0; d < g.D0; ++d) {
+          if (a.out_dtype == SAGE2_FP32)
+            static_cast<float *>(a.out)[o + d] = 0.f;
+          else
+            static_cast<uint16_t *>(a.out)[o + d] = 0;
+        }
+      }
+    return;
+  }
+
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::kBar);
+  uint64_t *q_full = bars;
+  uint64_t *kv_full = bars + 1;
+  uint64_t *kv_empty = kv_full + ST;
+  uint64_t *s_full = kv_empty + ST;  // [2] QK_t(j) complete
+  uint64_t *s_free = s_full + 2;     // [2] the softmax of tile t has read S_t(j)
+  uint64_t *p_full = s_free + 2;     // [2] P~_t(j) written, O_t rescaled
+  uint64_t *pv_done = p_full + 2;    // [2] PV_t(j) complete
+  uint64_t *drain = pv_done + 2;
+  uint64_t *tok = drain + 1;         // [2][4] tok[t][w]: the other tile's warp w finished logits
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kMisc + 4);
+  float *sv_s = reinterpret_cast<float *>(smem + P::kSv);
+
+  if (warp == kTmaWarp && lane == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 4);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&pv_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&tok[i], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 3) {  // the V channel scales for the epilogue
+    const float *svp = a.vscale + ((size_t)b * g.Hkv + hk) * DP;
+    for (int c = lane; c < DP; c += 32) sv_s[c] = __ldg(svp + c);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const AbortCtx ab{abort_flag, a.status};
+
+  if (warp < 4) {
+    regs_release<kPPRegsCtl>();
+    if (warp == kTmaWarp && lane == 0) {
+      // ---------------------------------------------------------- TMA producer (one lane)
+      const int yk0 = hk * a.L.Tkv + s.kvpad0;
+      const float *sk_row = a.kscale + (size_t)hk * (a.L.Tkv / kGK) + s.kvpad0 / kGK;
+      const float *dsc0 = a.dsc + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qtt[0]) * a.L.nkv_pad;
+      const float *dsc1 = dsc0 + a.L.nkv_pad;  // the next Q block's row
+      mbar_arrive_expect_tx(q_full, (valid[1] ? 2 : 1) * 128 * DP);
+      tma_load_2d(smem + P::kQ, &tm_q, 0, hq * a.L.Tq + s.qpad0 + qtt[0] * kBQ, q_full);
+      if (valid[1])
+        tma_load_2d(smem + P::kQ + 128 * DP, &tm_q, 0, hq * a.L.Tq + s.qpad0 + qtt[1] * kBQ,
+                    q_full);
+      int issued = 0;
+      for (int j = 0; j < Tmax; ++j) {
+        const int st = j % ST;
+        if (j >= ST && !mbar_wait<true>(&kv_empty[st], ((j / ST) - 1) & 1, ab, kSiteKvEmpty)) break;
+        const bool u0 = j < Tt[0], u1 = j < Tt[1];
+        mbar_arrive_expect_tx(&kv_full[st],
+                              128 * DP + DP * 128 + ((u0 ? 1 : 0) + (u1 ? 1 : 0)) * 512 + 16);
+        tma_load_2d(smem + P::kK + st * 128 * DP, &tm_k, 0, yk0 + j * kBKV, &kv_full[st]);
+        tma_load_2d(smem + P::kV + st * DP * 128, &tm_v, s.kvpad0 + j * kBKV, hk * DP,
+                    &kv_full[st]);
+        if (u0) bulk_load(smem + P::kDsc + st * 1024, dsc0 + (size_t)j * kBKV, 512, &kv_full[st]);
+        if (u1)
+          bulk_load(smem + P::kDsc + st * 1024 + 512, dsc1 + (size_t)j * kBKV, 512, &kv_full[st]);
+        bulk_load(smem + P::kSk + st * 16, sk_row + j * (kBKV / kGK), 16, &kv_full[st]);
+        issued = j + 1;
+      }
+      if (*abort_flag) {  // let the copies already issued land before the CTA exits
+        for (int n = issued > ST ? issued - ST : 0; n < issued; ++n)
+          drain_wait(&kv_full[n % ST], (n / ST) & 1);
+        drain_wait(q_full, 0);
+      }
+    } else if (warp == kMmaWarp && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer (one lane)
+      // QK_t(n) once S_t is free (the softmax read S_t(n-1)) and K(n) has landed; PV_t(n) once
+      // P~_t(n) is written; stage n is released once every MMA reading it has been issued.
+      constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
+      constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
+      bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
+      int nq0 = 0, nq1 = 0, np0 = 0, np1 = 0, ne = 0;
+      const int T0 = Tt[0], T1 = Tt[1];
+      uint64_t t_idle = 0;  // global time when the current idle spell was first checked
+      uint32_t idle = 0;    // polls without progress (the clock is read every 64th)
+      while (ok && (np0 < T0 || np1 < T1)) {
+        bool progress = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          int &nq = t ? nq1 : nq0;
+          int &np = t ? np1 : np0;
+          const int T = t ? T1 : T0;
+          if (np < nq && mbar_test_wait(&p_full[t], np & 1)) {
+            tc_fence_after();
+            const uint64_t pdesc = sdesc_kmajor(smem_u32(smem + P::kP + t * 16384), 128);
+            const uint64_t vdesc =
+                sdesc_kmajor(smem_u32(smem + P::kV + (np % ST) * DP * 128), 128);
+#pragma unroll
+            for (int kk = 0; kk < kBKV / 32; ++kk)
+              mma_e4m3_ss(tbase + pp_col_o(t), pdesc + (uint64_t)(kk * 2),
+                          vdesc + (uint64_t)(kk * 2), idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&pv_done[t]);
+            ++np;
+            progress = true;
+            // release every stage whose MMAs have all been issued
+            while (ne < Tmax && (ne >= T0 || np0 > ne) && (ne >= T1 || np1 > ne)) {
+              mma_commit(&kv_empty[ne % ST]);
+              ++ne;
+            }
+          }
+          if (nq < T && (nq == 0 || mbar_test_wait(&s_free[t], (nq - 1) & 1)) &&
+              mbar_test_wait(&kv_full[nq % ST], (nq / ST) & 1)) {
+            tc_fence_after();
+            const uint64_t adesc = sdesc_kmajor(smem_u32(smem + P::kQ + t * 128 * DP), DP);
+            const uint64_t kdesc =
+                sdesc_kmajor(smem_u32(smem + P::kK + (nq % ST) * 128 * DP), DP);
+#pragma unroll
+            for (int kk = 0; kk < DP / 32; ++kk)
+              mma_e4m3_ss(tbase + pp_col_s(t), adesc + (uint64_t)(kk * 2),
+                          kdesc + (uint64_t)(kk * 2), idesc_qk, kk > 0);
+            mma_commit(&s_full[t]);
+            ++nq;
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle = 0;
+        } else if ((++idle & 63u) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (idle == 64) t_idle = now;
+          if (*abort_flag) {
+            ok = false;
+          } else if (now - t_idle > SAGE2_WAIT_NS) {
+            *abort_flag = 1;
+            atomicCAS(a.status, 0, kStatusTimeoutBase | kSitePFull);
+            ok = false;
+          }
+        }
+      }
+      mma_commit(drain);  // every MMA issued above completes before tensor memory is freed
+      drain_wait(drain, 0);
+    }
+    cta_teardown(warp == kMmaWarp, tbase);
+  } else {
+    regs_acquire<kPPRegsSoftmax>();
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp < kFoldWarp0 ? 0 : 1;  // warps 4-7: tile 0, warps 8-11: tile 1
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
+    const int qt = qtt[t];
+    const int i = qt * kBQ + row;
+    const bool row_ok = valid[t] && i < s.nq;
+    const int T = Tt[t];
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const size_t o = ((size_t)(s.q0 + i) * g.Hq + hq) * g.D0;
+    if (valid[t] && T == 0) {  // no visible key in this tile
+      if (row_ok)
+        for (int d = 0; d < g.D0; ++d) {
+          if (a.out_dtype == SAGE2_FP32)
+            static_cast<float *>(a.out)[o + d] = 0.f;
+          else
+            static_cast<uint16_t *>(a.out)[o + d] = 0;
+        }
+    }
+    if (T > 0) {
+      const float c32 = g.c32;
+      const float sqc =
+          row_ok ? __fmul_rn(a.qscale[(size_t)hq * a.L.Tq + s.qpad0 + qt * kBQ + row], c32) : 0.f;
+      const int last_key = g.causal ? min(i + (s.nkv - s.nq), s.nkv - 1) : s.nkv - 1;
+      const float L32 = 8.8073549220576041f;  // fl32(log2(448))
+      const uint32_t tS = tbase + lane_base + pp_col_s(t);
+      const uint32_t tO = tbase + lane_base + pp_col_o(t);
+      // this thread's row of P~_t: 8 chunks of 16 bytes, chunk c at position c ^ (row & 7)
+      uint8_t *prow = smem + P::kP + t * 16384 + row * 128;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+#pragma unroll 1
+      for (int j = 0; j < T; ++j) {
+        const int st = j % ST;
+        ok = warp_all(mbar_wait(&s_full[t], j & 1, ab, kSiteSFull));
+        if (!ok) break;
+        // my turn for the logits phase: tile 0 waits for tile 1's logits(j-1), tile 1 for tile
+        // 0's logits(j) (only while the other tile still has those tiles)
+        if (t == 0 ? (j >= 1 && j - 1 < Tt[1]) : (j < Tt[0])) {
+          ok = warp_all(mbar_wait(&tok[t * 4 + qd], (t == 0 ? j - 1 : j) & 1, ab, kSiteTok));
+          if (!ok) break;
+        }
+        tc_fence_after();
+        uint32_t v[128];
+        tmem_ld128_nowait(tS, v);
+        const bool kv_ready = mbar_try_wait(&kv_full[st], (j / ST) & 1);
+        tmem_wait_ld128(v);  // S_t(j) is in registers: QK_t(j+1) may overwrite S_t
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[t]);
+        ok = warp_all(kv_ready || mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm));
+        if (!ok) break;
+        const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 1024 + t * 512);
+        const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
+        const int lim = last_key - j * kBKV;
+        float x[128];
+        float pmax = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float xh[64];
+          uint32_t vh[64];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) vh[e] = v[64 * h + e];
+          pmax = fmaxf(pmax, logits64<true>(xh, vh, dsc + 64 * h, skv + 2 * h, sqc, lim - 64 * h));
+#pragma unroll
+          for (int e = 0; e < 64; ++e) x[64 * h + e] = xh[e];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tok[(1 - t) * 4 + qd]);  // the other tile's turn
+        const float m_new = fmaxf(m, pmax);
+        const bool none = (m_new == -INFINITY);
+        const float alpha = none ? 1.f : ex2_approx(__fsub_rn(m, m_new));
+        const float m448 = none ? 0.f : __fsub_rn(m_new, L32);
+#pragma unroll
+        for (int e = 0; e < 128; e += 2) add2(x[e], x[e + 1], x[e], x[e + 1], -m448, -m448);
+#pragma unroll
+        for (int e = 0; e < 128; ++e) x[e] = ex2_approx(x[e]);
+        float ps[4][2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ps[k][0] = ps[k][1] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 128; e += 2)
+          add2(ps[(e >> 1) & 3][0], ps[(e >> 1) & 3][1], ps[(e >> 1) & 3][0], ps[(e >> 1) & 3][1],
+               x[e], x[e + 1]);
+        const float rs = __fadd_rn(
+            __fadd_rn(__fadd_rn(ps[0][0], ps[0][1]), __fadd_rn(ps[1][0], ps[1][1])),
+            __fadd_rn(__fadd_rn(ps[2][0], ps[2][1]), __fadd_rn(ps[3][0], ps[3][1])));
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          pk[e] = cvt_e4m3x2(x[4 * e], x[4 * e + 1]) | (cvt_e4m3x2(x[4 * e + 2], x[4 * e + 3]) << 16);
+        if (j > 0) {
+          // PV_t(j-1) complete: O_t holds the sum through tile j-1 and P~_t may be rewritten
+          ok = warp_all(mbar_wait(&pv_done[t], (j - 1) & 1, ab, kSitePvDone));
+          if (!ok) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {  // O = alpha O (one load, one wait)
+            uint32_t ov[DP];
+            if constexpr (DP == 128) {
+              tmem_ld128_nowait(tO, ov);
+              tmem_wait_ld128(ov);
+            } else {
+              tmem_ld64(tO, ov);
+            }
+#pragma unroll
+            for (int c = 0; c < DP / 32; ++c) {
+              uint32_t r[32];
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float y0, y1;
+                mul2(y0, y1, __uint_as_float(ov[32 * c + e]), __uint_as_float(ov[32 * c + e + 1]),
+                     alpha, alpha);
+                r[e] = __float_as_uint(y0);
+                r[e + 1] = __float_as_uint(y1);
+              }
+              tmem_st32(tO + 32 * c, r);
+            }
+            tmem_st_wait();
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_async_smem();  // the generic-proxy stores become visible to the MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
+        l = __fmaf_rn(alpha, l, rs);
+        m = m_new;
+      }
+      // ---------------------------------------------------------- epilogue
+      if (ok) ok = warp_all(mbar_wait(&pv_done[t], (T - 1) & 1, ab, kSitePvDone));
+      if (warp_all(ok && !*abort_flag)) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
+#pragma unroll
+        for (int c = 0; c < DP / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_wait(tO + 32 * c, r);
+#pragma unroll
+          for (int e8 = 0; e8 < 32; e8 += 8) {
+            const int d = 32 * c + e8;
+            if (row_ok && d < g.D0) {
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                y[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[e8 + e]), sv_s[d + e]), inv_l);
+              if (a.out_dtype == SAGE2_FP32) {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + o + d);
+                dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+                dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+              } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  uint16_t lo, hi;
+                  if (a.out_dtype == SAGE2_BF16) {
+                    lo = __bfloat16_as_ushort(__float2bfloat16_rn(y[2 * e]));
+                    hi = __bfloat16_as_ushort(__float2bfloat16_rn(y[2 * e + 1]));
+                  } else {
+                    lo = __half_as_ushort(__float2half_rn(y[2 * e]));
+                    hi = __half_as_ushort(__float2half_rn(y[2 * e + 1]));
+                  }
+                  w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + o + d) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+        }
+      }
+    }
+    cta_teardown(false, tbase);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -638,6 +1054,33 @@ cudaError_t launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnArg
   return cudaGetLastError();
 }
 
+template <int DP, int ST>
+cudaError_t launch_pp(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                      const AttnArgs &a, dim3 grid, cudaStream_t st) {
+  using P = PPPlan<DP, ST>;
+  constexpr int kSmem = P::kBytes > 116 * 1024 ? P::kBytes : 116 * 1024;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_pp<DP, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  attn_pp<DP, ST><<<grid, kThreads, kSmem, st>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+// The two-tile kernel is selected with SAGE2_ATTN_PP=1 (INT4 codes, no debug hook).
+bool use_pp() {
+  static int v = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char *e = getenv("SAGE2_ATTN_PP");
+    v = (e && e[0] == '1') ? 1 : 0;
+  });
+  return v == 1;
+}
+
 }  // namespace
 
 cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const Layout &L,
@@ -667,6 +1110,14 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
                           CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int nqt = (g.max_nq + kBQ - 1) / kBQ;
+  if (!int8_qk && !dbg && use_pp()) {
+    CUtensorMap mq;
+    if (!make_map(&mq, w.qcode, g.Dp, (uint64_t)g.Hq * L.Tq, g.Dp, 128, qk_sw))
+      return cudaErrorInvalidValue;
+    const dim3 grid2((nqt + 1) / 2, g.Hq, g.B);
+    if (g.Dp == 128) return launch_pp<128, 4>(mq, mk, mv, a, grid2, st);
+    return launch_pp<64, 8>(mq, mk, mv, a, grid2, st);
+  }
   const dim3 grid = dbg ? dim3(1) : dim3(nqt, g.Hq, g.B);
   // pipeline depth: as many K/V stages as fit (a stage of fp16 K codes is twice as large)
   if (int8_qk) {

@@ -62,6 +62,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test: never suspends the thread (for a waiter that polls several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Same test with a suspend-time hint: a thread whose phase is not complete sleeps (up to
 // `ns` nanoseconds, or until the phase completes) instead of retrying at once, which leaves the
 // shared-memory instruction path to the other warps of its sub-partition. Wake-up is slower, so
