@@ -50,9 +50,9 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # the kernel source they were taken on (sha256 prefix of csrc/sage2_attention.cu).
 MEASURED_TRAFFIC = {
     ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage2"): (
-        "74c005a605d43bd1", 745.38e6 + 246.30e6),
+        "2cca362ee3c101b8", 746.78e6 + 246.43e6),
     ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage1"): (
-        "74c005a605d43bd1", 374.60e6 + 233.44e6),
+        "2cca362ee3c101b8", 374.18e6 + 234.03e6),
 }
 
 
@@ -383,7 +383,9 @@ def run_ours(args, rank, world, local):
     achieved = ops / (att_mean / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": measured_traffic(w, args.quant), "kernel": "attn_fwd",
+                "traffic": measured_traffic(w, args.quant),
+                "kernel": "attn_fwd" if sage1 or os.environ.get("SAGE2_ATTN_PP") == "0"
+                else "attn_pp",
                 "peak_source": (f"{peak_src} bf16 burst x {mix:.4g} (Q K^T f16, P~V e4m3, "
                                 "time-weighted)" if sage1 else
                                 f"{peak_src} bf16 burst x {FP8_OVER_BF16} (e4m3)"),

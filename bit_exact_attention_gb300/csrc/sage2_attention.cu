@@ -605,15 +605,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DP, int ST>
 struct PPPlan {
   static constexpr int kQ = 0;                       // [2][128 rows][DP]   (swizzled)
-  static constexpr int kP = kQ + 2 * 128 * DP;       // [2][128 rows][128]  (128B swizzled)
-  static constexpr int kK = kP + 2 * 128 * 128;      // [ST][128 keys][DP]  (swizzled)
+  static constexpr int kP = kQ + 2 * 128 * DP;       // [2 tiles][2][128][128] (128B swizzled)
+  static constexpr int kK = kP + 4 * 128 * 128;      // [ST][128 keys][DP]  (swizzled)
   static constexpr int kV = kK + ST * 128 * DP;      // [ST][DP][128 keys]  (swizzled)
   static constexpr int kDsc = kV + ST * DP * 128;    // float [ST][2][128]
   static constexpr int kSk = kDsc + ST * 2 * 512;    // float [ST][4]
   static constexpr int kSv = kSk + ST * 16;          // float [DP]
   static constexpr int kBar = kSv + DP * 4;
-  // q, full[ST], empty[ST], s_full[2], s_free[2], p_full[2], pv_done[2], drain, tok[2][4]
-  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 2 + 2 + 1 + 8;
+  // q, full[ST], empty[ST], s_full[2], s_free[2], p_full[2][2], pv_done[2], drain, tok[2][4]
+  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 4 + 2 + 1 + 8;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kBytes = kEnd + 1024;
@@ -675,8 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *kv_empty = kv_full + ST;
   uint64_t *s_full = kv_empty + ST;  // [2] QK_t(j) complete
   uint64_t *s_free = s_full + 2;     // [2] the softmax of tile t has read S_t(j)
-  uint64_t *p_full = s_free + 2;     // [2] P~_t(j) written, O_t rescaled
-  uint64_t *pv_done = p_full + 2;    // [2] PV_t(j) complete
+  uint64_t *p_full = s_free + 2;     // [2][2] P~_t(j) written into buffer j % 2, O_t rescaled
+  uint64_t *pv_done = p_full + 4;    // [2] PV_t(j) complete
   uint64_t *drain = pv_done + 2;
   uint64_t *tok = drain + 1;         // [2][4] tok[t][w]: the other tile's warp w finished logits
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::kMisc);
@@ -692,7 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&s_free[t], 4);
-      mbar_init(&p_full[t], 4);
+      mbar_init(&p_full[2 * t], 4);
+      mbar_init(&p_full[2 * t + 1], 4);
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -769,9 +770,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           int &nq = t ? nq1 : nq0;
           int &np = t ? np1 : np0;
           const int T = t ? T1 : T0;
-          if (np < nq && mbar_test_wait(&p_full[t], np & 1)) {
+          if (np < nq && mbar_test_wait(&p_full[2 * t + (np & 1)], (np >> 1) & 1)) {
             tc_fence_after();
-            const uint64_t pdesc = sdesc_kmajor(smem_u32(smem + P::kP + t * 16384), 128);
+            const uint64_t pdesc =
+                sdesc_kmajor(smem_u32(smem + P::kP + (2 * t + (np & 1)) * 16384), 128);
             const uint64_t vdesc =
                 sdesc_kmajor(smem_u32(smem + P::kV + (np % ST) * DP * 128), 128);
 #pragma unroll
@@ -787,7 +789,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++ne;
             }
           }
-          if (nq < T && (nq == 0 || mbar_test_wait(&s_free[t], (nq - 1) & 1)) &&
+          // QK_t(nq) after PV_t(nq-2): its commit then also covers PV_t(nq-2), which frees the
+          // P~ buffer that the softmax of tile nq refills
+          if (nq < T && np >= nq - 1 && (nq == 0 || mbar_test_wait(&s_free[t], (nq - 1) & 1)) &&
               mbar_test_wait(&kv_full[nq % ST], (nq / ST) & 1)) {
             tc_fence_after();
             const uint64_t adesc = sdesc_kmajor(smem_u32(smem + P::kQ + t * 128 * DP), DP);
@@ -849,8 +853,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float L32 = 8.8073549220576041f;  // fl32(log2(448))
       const uint32_t tS = tbase + lane_base + pp_col_s(t);
       const uint32_t tO = tbase + lane_base + pp_col_o(t);
-      // this thread's row of P~_t: 8 chunks of 16 bytes, chunk c at position c ^ (row & 7)
-      uint8_t *prow = smem + P::kP + t * 16384 + row * 128;
+      // this thread's row of P~_t(j) in buffer j % 2: 8 chunks of 16 bytes, chunk c at position
+      // c ^ (row & 7)
+      uint8_t *prow0 = smem + P::kP + 2 * t * 16384 + row * 128;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
 #pragma unroll 1
@@ -913,35 +918,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
           pk[e] = cvt_e4m3x2(x[4 * e], x[4 * e + 1]) | (cvt_e4m3x2(x[4 * e + 2], x[4 * e + 3]) << 16);
-        if (j > 0) {
-          // PV_t(j-1) complete: O_t holds the sum through tile j-1 and P~_t may be rewritten
+        // O = alpha O once PV_t(j-1) has added its partial; with every alpha of the warp's rows
+        // equal to 1 there is nothing to wait for, except on the last tile: pv_done_t may then
+        // lag two phases behind (only QK_t(j) complete implies PV_t(j-2)), and the wait for
+        // PV_t(j-1) here keeps the epilogue's parity wait for PV_t(T-1) unambiguous
+        const bool resc = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+        if (resc || (j > 0 && j == T - 1)) {
           ok = warp_all(mbar_wait(&pv_done[t], (j - 1) & 1, ab, kSitePvDone));
           if (!ok) break;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {  // O = alpha O (one load, one wait)
-            uint32_t ov[DP];
-            if constexpr (DP == 128) {
-              tmem_ld128_nowait(tO, ov);
-              tmem_wait_ld128(ov);
-            } else {
-              tmem_ld64(tO, ov);
-            }
+          if (resc) {
 #pragma unroll
-            for (int c = 0; c < DP / 32; ++c) {
-              uint32_t r[32];
+            for (int h = 0; h < DP / 64; ++h) {  // 64 columns per load
+              uint32_t ov[64];
+              tmem_ld64(tO + 64 * h, ov);
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                float y0, y1;
-                mul2(y0, y1, __uint_as_float(ov[32 * c + e]), __uint_as_float(ov[32 * c + e + 1]),
-                     alpha, alpha);
-                r[e] = __float_as_uint(y0);
-                r[e + 1] = __float_as_uint(y1);
+              for (int c = 0; c < 2; ++c) {
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  float y0, y1;
+                  mul2(y0, y1, __uint_as_float(ov[32 * c + e]), __uint_as_float(ov[32 * c + e + 1]),
+                       alpha, alpha);
+                  r[e] = __float_as_uint(y0);
+                  r[e + 1] = __float_as_uint(y1);
+                }
+                tmem_st32(tO + 64 * h + 32 * c, r);
               }
-              tmem_st32(tO + 32 * c, r);
             }
             tmem_st_wait();
           }
         }
+        // buffer j % 2 is free: PV_t(j-2) was issued before QK_t(j), whose completion (s_full)
+        // implies it
+        uint8_t *prow = prow0 + (j & 1) * 16384;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
@@ -949,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_smem();  // the generic-proxy stores become visible to the MMA
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[t]);
+        if (lane == 0) mbar_arrive(&p_full[2 * t + (j & 1)]);
         l = __fmaf_rn(alpha, l, rs);
         m = m_new;
       }
@@ -1070,15 +1080,12 @@ cudaError_t launch_pp(const CUtensorMap &mq, const CUtensorMap &mk, const CUtens
   return cudaGetLastError();
 }
 
-// The two-tile kernel is selected with SAGE2_ATTN_PP=1 (INT4 codes, no debug hook).
+// INT4 codes run on the two-tile kernel; SAGE2_ATTN_PP=0 in the environment selects the
+// one-tile kernel instead (which also serves the INT8 path and the debug hook). Read at every
+// launch, so a process can compare the two.
 bool use_pp() {
-  static int v = -1;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    const char *e = getenv("SAGE2_ATTN_PP");
-    v = (e && e[0] == '1') ? 1 : 0;
-  });
-  return v == 1;
+  const char *e = getenv("SAGE2_ATTN_PP");
+  return !(e && e[0] == '0');
 }
 
 }  // namespace
@@ -1115,8 +1122,8 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
     if (!make_map(&mq, w.qcode, g.Dp, (uint64_t)g.Hq * L.Tq, g.Dp, 128, qk_sw))
       return cudaErrorInvalidValue;
     const dim3 grid2((nqt + 1) / 2, g.Hq, g.B);
-    if (g.Dp == 128) return launch_pp<128, 4>(mq, mk, mv, a, grid2, st);
-    return launch_pp<64, 8>(mq, mk, mv, a, grid2, st);
+    if (g.Dp == 128) return launch_pp<128, 3>(mq, mk, mv, a, grid2, st);
+    return launch_pp<64, 6>(mq, mk, mv, a, grid2, st);
   }
   const dim3 grid = dbg ? dim3(1) : dim3(nqt, g.Hq, g.B);
   // pipeline depth: as many K/V stages as fit (a stage of fp16 K codes is twice as large)

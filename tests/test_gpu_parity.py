@@ -161,6 +161,22 @@ def test_forward_matches_emulation_fp32(name):
     assert abs(mg["cos"] - mq["cos"]) <= 1e-4, (mg, mq)
 
 
+@pytest.mark.parametrize("name", list(SCALED))
+def test_one_tile_kernel_matches_emulation(name, monkeypatch):
+    """The method's codes on the one-tile kernel (fresh FP32 partial per key tile, FP32 fold in
+    registers), which SAGE2_ATTN_PP=0 selects, hold the same gate as the default two-tile kernel
+    (FP32 rescale, then the P~V MMA accumulating into O); the two agree to the same tolerance."""
+    w, x, g = run_case(name)
+    default = g.forward(out_dtype=torch.float32).cpu().numpy()
+    monkeypatch.setenv("SAGE2_ATTN_PP", "0")
+    out = g.forward(out_dtype=torch.float32).cpu().numpy()
+    assert g.status() == (0, 0)
+    m = metrics(out, oracle_ref(w, x))
+    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+    m2 = metrics(out, default)
+    assert m2["relL1"] <= REL_L1 and m2["maxabs"] <= MAX_ABS, m2
+
+
 @pytest.mark.parametrize("name", ["tiny", "prefill", "varlen"])
 def test_forward_low_precision_output(name):
     w, x, g = run_case(name)
@@ -216,8 +232,11 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("kernel", ["two_tile", "one_tile"])
 @pytest.mark.parametrize("case", EDGE, ids=[f"e{i}" for i in range(len(EDGE))])
-def test_edge_cases(case):
+def test_edge_cases(case, kernel, monkeypatch):
+    if kernel == "one_tile":
+        monkeypatch.setenv("SAGE2_ATTN_PP", "0")
     nq, nkv, hq, hkv, d, causal, dt = case
     w = W.Workload("edge", nq, nkv, hq, hkv, d, dt, causal, "kbias9", 31, varlen=True)
     x = W.make_inputs(w)
