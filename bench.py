@@ -50,9 +50,9 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # the kernel source they were taken on (sha256 prefix of csrc/sage2_attention.cu).
 MEASURED_TRAFFIC = {
     ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage2"): (
-        "2cca362ee3c101b8", 746.78e6 + 246.43e6),
+        "1a1f25f1839a8e84", 745.71e6 + 246.36e6),
     ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage1"): (
-        "2cca362ee3c101b8", 374.18e6 + 234.03e6),
+        "1a1f25f1839a8e84", 374.54e6 + 233.73e6),
 }
 
 

@@ -1,6 +1,10 @@
-// sage2_attention.cu -- the fused SageAttention2 attention kernel for sm_103a.
+// sage2_attention.cu -- the fused SageAttention2 attention kernels for sm_103a.
 //
-// One CTA per (sequence, q head, 128-row Q tile); twelve warps in three warpgroups:
+// Two kernels share the helpers below. attn_pp (further down) computes two 128-row Q tiles per
+// CTA and runs the method's INT4 codes. attn_fwd, described first, computes one tile per CTA and
+// runs the INT8-code path, the debug hook, and the INT4 codes when SAGE2_ATTN_PP=0.
+//
+// attn_fwd: one CTA per (sequence, q head, 128-row Q tile); twelve warps in three warpgroups:
 //   warp 0      TMA producer (one lane): per KV tile the K codes, the transposed V codes,
 //               128 DeltaS*c values and 4 K scales into an ST-stage ring.
 //   warps 1, 2  MMA issuers (one lane each), tcgen05 kind::f8f6f4 (e4m3 x e4m3 -> f32), A from
@@ -863,12 +867,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % ST;
         ok = warp_all(mbar_wait(&s_full[t], j & 1, ab, kSiteSFull));
         if (!ok) break;
-        // my turn for the logits phase: tile 0 waits for tile 1's logits(j-1), tile 1 for tile
-        // 0's logits(j) (only while the other tile still has those tiles)
-        if (t == 0 ? (j >= 1 && j - 1 < Tt[1]) : (j < Tt[0])) {
-          ok = warp_all(mbar_wait(&tok[t * 4 + qd], (t == 0 ? j - 1 : j) & 1, ab, kSiteTok));
-          if (!ok) break;
-        }
         tc_fence_after();
         uint32_t v[128];
         tmem_ld128_nowait(tS, v);
@@ -879,6 +877,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&s_free[t]);
         ok = warp_all(kv_ready || mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm));
         if (!ok) break;
+        // my turn for the logits phase (S is already loaded and released): tile 0 waits for
+        // tile 1's logits(j-1), tile 1 for tile 0's logits(j) (only while the other tile still
+        // has those tiles)
+        if (t == 0 ? (j >= 1 && j - 1 < Tt[1]) : (j < Tt[0])) {
+          ok = warp_all(mbar_wait(&tok[t * 4 + qd], (t == 0 ? j - 1 : j) & 1, ab, kSiteTok));
+          if (!ok) break;
+        }
         const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 1024 + t * 512);
         const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
         const int lim = last_key - j * kBKV;
