@@ -240,7 +240,9 @@ def device_status(workspace, stream=None) -> tuple[int, int]:
 def debug_tile(workspace, B, Hq, Hkv, max_nq, max_nkv, D, causal, b, h, qt, kt, sm_scale=0.0,
                cu_seqlens_q=None, cu_seqlens_kv=None, total_q=None, total_kv=None, stream=None,
                quant_flags=0):
-    """Raw (S accumulators, P~ bytes, fresh P~V partial) of one KV tile of one work unit."""
+    """Raw (S accumulators, P~ bytes, fresh P~V partial) of one KV tile of one work unit. On
+    the two-tile kernel (INT4 codes) the partial is returned for kt = 0 only (zeros otherwise);
+    see sage2_debug_tile in include/sage2_attn.h."""
     dev = workspace.device
     Dp = 64 if D <= 64 else 128
     s_out = torch.zeros(128, 128, dtype=torch.float32, device=dev)

@@ -631,7 +631,10 @@ static_assert(kPPRegsCtl + 2 * kPPRegsSoftmax <= 3 * kRegsLaunch, "register spli
 __device__ __forceinline__ uint32_t pp_col_s(int t) { return (uint32_t)t * 256u; }
 __device__ __forceinline__ uint32_t pp_col_o(int t) { return (uint32_t)t * 256u + 128u; }
 
-template <int DP, int ST>
+// DBG: one CTA, the pair holding Q tile a.dbg.qt of (sequence a.dbg.b, head a.dbg.h); the
+// softmax warps of that tile dump S(kt) (the raw integer accumulators) and P~(kt), and for
+// kt = 0 the first block partial P~(0) V(0), which is O after PV(0).
+template <int DP, int ST, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_pp(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -641,8 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Geometry &g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int format = a.status[1];
-  const int b = blockIdx.z, hq = blockIdx.y;
-  const int pair = g.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int b = DBG ? a.dbg.b : (int)blockIdx.z, hq = DBG ? a.dbg.h : (int)blockIdx.y;
+  const int pair = DBG ? a.dbg.qt / 2
+                       : (g.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
   if (format != kFormatInt4) {
     if (tid == 0) atomicCAS(a.status, 0, kStatusFormat);
@@ -872,6 +876,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld128_nowait(tS, v);
         const bool kv_ready = mbar_try_wait(&kv_full[st], (j / ST) & 1);
         tmem_wait_ld128(v);  // S_t(j) is in registers: QK_t(j+1) may overwrite S_t
+        const bool dump = DBG && t == (a.dbg.qt & 1) && j == a.dbg.kt;
+        if (dump) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e) a.dbg.s_out[row * 128 + e] = __uint_as_float(v[e]);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[t]);
@@ -923,6 +932,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
           pk[e] = cvt_e4m3x2(x[4 * e], x[4 * e + 1]) | (cvt_e4m3x2(x[4 * e + 2], x[4 * e + 3]) << 16);
+        if (dump) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            *reinterpret_cast<uint32_t *>(a.dbg.p_out + row * 128 + 4 * e) = pk[e];
+        }
         // O = alpha O once PV_t(j-1) has added its partial; with every alpha of the warp's rows
         // equal to 1 there is nothing to wait for, except on the last tile: pv_done_t may then
         // lag two phases behind (only QK_t(j) complete implies PV_t(j-2)), and the wait for
@@ -965,6 +979,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[2 * t + (j & 1)]);
+        if (dump && j == 0) {  // O after PV(0) is the fresh partial P~(0) V(0)
+          ok = warp_all(mbar_wait(&pv_done[t], 0, ab, kSitePvDone));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < DP / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32_wait(tO + 32 * c, r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a.dbg.r_out[row * DP + 32 * c + e] = __uint_as_float(r[e]);
+          }
+        }
         l = __fmaf_rn(alpha, l, rs);
         m = m_new;
       }
@@ -1069,7 +1095,7 @@ cudaError_t launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnArg
   return cudaGetLastError();
 }
 
-template <int DP, int ST>
+template <int DP, int ST, bool DBG>
 cudaError_t launch_pp(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                       const AttnArgs &a, dim3 grid, cudaStream_t st) {
   using P = PPPlan<DP, ST>;
@@ -1077,17 +1103,17 @@ cudaError_t launch_pp(const CUtensorMap &mq, const CUtensorMap &mk, const CUtens
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_pp<DP, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmem);
+    attr_err = cudaFuncSetAttribute(attn_pp<DP, ST, DBG>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attn_pp<DP, ST><<<grid, kThreads, kSmem, st>>>(mq, mk, mv, a);
+  attn_pp<DP, ST, DBG><<<grid, kThreads, kSmem, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
-// INT4 codes run on the two-tile kernel; SAGE2_ATTN_PP=0 in the environment selects the
-// one-tile kernel instead (which also serves the INT8 path and the debug hook). Read at every
-// launch, so a process can compare the two.
+// INT4 codes run on the two-tile kernel (the debug hook too, except the unit whose producer
+// issues nothing); SAGE2_ATTN_PP=0 in the environment selects the one-tile kernel instead, which
+// also serves the INT8 path. Read at every launch, so a process can compare the two.
 bool use_pp() {
   const char *e = getenv("SAGE2_ATTN_PP");
   return !(e && e[0] == '0');
@@ -1122,13 +1148,17 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
                           CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int nqt = (g.max_nq + kBQ - 1) / kBQ;
-  if (!int8_qk && !dbg && use_pp()) {
+  if (!int8_qk && !(dbg && dbg->skip_loads) && use_pp()) {
     CUtensorMap mq;
     if (!make_map(&mq, w.qcode, g.Dp, (uint64_t)g.Hq * L.Tq, g.Dp, 128, qk_sw))
       return cudaErrorInvalidValue;
+    if (dbg) {
+      if (g.Dp == 128) return launch_pp<128, 3, true>(mq, mk, mv, a, dim3(1), st);
+      return launch_pp<64, 6, true>(mq, mk, mv, a, dim3(1), st);
+    }
     const dim3 grid2((nqt + 1) / 2, g.Hq, g.B);
-    if (g.Dp == 128) return launch_pp<128, 3>(mq, mk, mv, a, grid2, st);
-    return launch_pp<64, 6>(mq, mk, mv, a, grid2, st);
+    if (g.Dp == 128) return launch_pp<128, 3, false>(mq, mk, mv, a, grid2, st);
+    return launch_pp<64, 6, false>(mq, mk, mv, a, grid2, st);
   }
   const dim3 grid = dbg ? dim3(1) : dim3(nqt, g.Hq, g.B);
   // pipeline depth: as many K/V stages as fit (a stage of fp16 K codes is twice as large)

@@ -211,8 +211,12 @@ int sage2_workspace_layout_ex(int B, int Hq, int Hkv, int max_Nq, int max_Nkv, i
  * q tile qt) work unit on a prepared workspace and dumps, for its KV tile kt, the raw
  * integer Q K^T accumulators (s_out: f32 [128][128], exact integers), the P~ e4m3 bytes
  * (p_out: u8 [128][128]) and the fresh P~V partial (r_out: f32 [128][Dp]), all device
- * buffers. Same size arguments as sage2_attention_varlen (cu_seqlens may be NULL for dense
- * inputs, then Nq = max_Nq and Nkv = max_Nkv for every sequence). */
+ * buffers. The two-tile kernel that runs the INT4 codes accumulates P~V straight into the
+ * output accumulator, so there r_out is written for kt = 0 only (the first partial) and left
+ * untouched otherwise; with SAGE2_ATTN_PP=0 in the environment, and for INT8 codes, the
+ * one-tile kernel runs and r_out is written for every kt. Same size arguments as
+ * sage2_attention_varlen (cu_seqlens may be NULL for dense inputs, then Nq = max_Nq and
+ * Nkv = max_Nkv for every sequence). */
 int sage2_debug_tile(const int *cu_seqlens_q, const int *cu_seqlens_kv, int B, int Hq, int Hkv,
                      int max_Nq, int max_Nkv, int total_q, int total_kv, int D, int causal,
                      float sm_scale, const void *workspace, size_t workspace_bytes, int b, int h,
