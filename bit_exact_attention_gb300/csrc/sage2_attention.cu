@@ -1,8 +1,9 @@
 // sage2_attention.cu -- the fused SageAttention2 attention kernels for sm_103a.
 //
 // Two kernels share the helpers below. attn_pp (further down) computes two 128-row Q tiles per
-// CTA and runs the method's INT4 codes. attn_fwd, described first, computes one tile per CTA and
-// runs the INT8-code path, the debug hook, and the INT4 codes when SAGE2_ATTN_PP=0.
+// CTA and runs the method's INT4 codes, and their debug dumps. attn_fwd, described first,
+// computes one tile per CTA. It runs the INT8-code path, the debug unit whose producer issues
+// nothing, and the INT4 codes when SAGE2_ATTN_PP=0.
 //
 // attn_fwd: one CTA per (sequence, q head, 128-row Q tile); twelve warps in three warpgroups:
 //   warp 0      TMA producer (one lane): per KV tile the K codes, the transposed V codes,

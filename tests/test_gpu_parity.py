@@ -173,7 +173,10 @@ def test_forward_matches_emulation_fp32(name):
 def test_one_tile_kernel_matches_emulation(name, monkeypatch):
     """The method's codes on the one-tile kernel (fresh FP32 partial per key tile, FP32 fold in
     registers), which SAGE2_ATTN_PP=0 selects, hold the same gate as the default two-tile kernel
-    (FP32 rescale, then the P~V MMA accumulating into O); the two agree to the same tolerance."""
+    (FP32 rescale, then the P~V MMA accumulating into O). Both compute the same P~ codes and row
+    sums, so the outputs differ only by where the accumulation rounds: at FP32 level (measured
+    2^-20.9 of max|O| at worst on these cases). An accumulator with a 13-bit significand, the
+    flaw the two-level scheme repairs, would put the difference near 2^-13."""
     w, x, g = run_case(name)
     default = g.forward(out_dtype=torch.float32).cpu().numpy()
     monkeypatch.setenv("SAGE2_ATTN_PP", "0")
@@ -181,8 +184,9 @@ def test_one_tile_kernel_matches_emulation(name, monkeypatch):
     assert g.status() == (0, 0)
     m = metrics(out, oracle_ref(w, x))
     assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
-    m2 = metrics(out, default)
-    assert m2["relL1"] <= REL_L1 and m2["maxabs"] <= MAX_ABS, m2
+    m2 = metrics(default, out)
+    scale = float(np.abs(out).max()) if out.size else 0.0
+    assert m2["relL1"] <= 1e-6 and m2["maxabs"] <= 2.0 ** -18 * max(scale, 1e-30), m2
 
 
 @pytest.mark.parametrize("name", ["tiny", "prefill", "varlen"])
