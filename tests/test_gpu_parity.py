@@ -268,6 +268,47 @@ def test_edge_cases(case, kernel, monkeypatch):
                 assert np.all(out[x["cu_q"][b] + i] == 0)
 
 
+def _random_shapes(n, seed):
+    """Seeded ragged problems: 1-3 sequences (empty ones included, the first never empty),
+    GQA ratios 1-4, head dims padded to 64 or 128, causal or not."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for _ in range(n):
+        nb = int(rng.integers(1, 4))
+        nq = tuple(int(rng.integers(0 if b else 1, 900)) for b in range(nb))
+        nkv = tuple(int(rng.integers(0 if b else 1, 1500)) for b in range(nb))
+        hkv = int(rng.choice([1, 2, 4]))
+        hq = hkv * int(rng.choice([1, 2, 4]))
+        d = int(rng.choice([40, 64, 96, 128]))
+        shapes.append((nq, nkv, hq, hkv, d, bool(rng.integers(0, 2)),
+                       "bf16" if rng.integers(0, 2) else "fp16"))
+    return shapes
+
+
+RANDOM_SHAPES = _random_shapes(16, 2024)
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM_SHAPES)))
+def test_two_tile_kernel_agrees_with_one_tile_on_random_shapes(i, monkeypatch):
+    """Ragged pairings (a second tile that is empty or sees fewer key tiles, pairs past the end of
+    a sequence, sequences with no keys) on the two-tile kernel, against the one-tile kernel: both
+    quantize identically, so the outputs agree to FP32 accumulation level and masked rows are 0
+    on both."""
+    nq, nkv, hq, hkv, d, causal, dt = RANDOM_SHAPES[i]
+    w = W.Workload("rand", nq, nkv, hq, hkv, d, dt, causal, "kbias9", 100 + i, varlen=True)
+    x = W.make_inputs(w)
+    g = GpuCase(w, x)
+    a = g.forward(out_dtype=torch.float32).double().cpu().numpy()
+    assert g.status() == (0, 0)
+    monkeypatch.setenv("SAGE2_ATTN_PP", "0")
+    b = g.forward(out_dtype=torch.float32).double().cpu().numpy()
+    assert g.status() == (0, 0)
+    assert np.all(np.isfinite(a))
+    scale = float(np.abs(b).max()) if b.size else 0.0
+    assert np.abs(a - b).max(initial=0.0) <= 2.0 ** -18 * max(scale, 1e-30), (
+        RANDOM_SHAPES[i], float(np.abs(a - b).max(initial=0.0)), scale)
+
+
 def test_sm_scale_argument():
     w = W.scaled(W.TINY, (200,), (300,), hq=2, hkv=2)
     x = W.make_inputs(w)
