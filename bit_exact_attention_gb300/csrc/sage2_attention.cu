@@ -597,11 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // SM sub-partition runs one softmax warp of each tile, so one tile's arithmetic fills the
 // other's MMA latency).
 // Per tile t: tensor memory S_t [256 t, 256 t + 128) and O_t [256 t + 128, 256 t + 128 + DP) (the
-// FP32 output accumulator); Q_t codes and P~_t (128 x 128 e4m3, the A operand of P~V) in shared
-// memory, 128-byte swizzled K-major. Per KV tile j the softmax loads S_t(j) into registers and
-// releases S_t at once (QK_t(j+1) may start), computes P~_t(j), waits for PV_t(j-1), rescales
-// O_t by alpha(j) (skipped when every row of the warp has alpha = 1), writes P~_t(j) and hands
-// it to the issuer; PV_t(j) then adds the block partial P~(j) V(j) into O_t.
+// FP32 output accumulator); Q_t codes and two P~_t buffers (128 x 128 e4m3, the A operand of
+// P~V) in shared memory, 128-byte swizzled K-major. Per KV tile j the softmax loads S_t(j) into
+// registers and releases S_t at once (QK_t(j+1) may start) and computes P~_t(j). If a row maximum
+// of the warp moved, it waits for PV_t(j-1) and rescales O_t by alpha(j). It writes P~_t(j) into
+// buffer j % 2 and hands it to the issuer; PV_t(j) then adds the block partial P~(j) V(j) into
+// O_t.
 // The issuer is event driven: it issues whichever of QK_0, PV_0, QK_1, PV_1 is ready.
 // The softmax warps of the two tiles that share a sub-partition take turns on the logits phase
 // (ALU bound: dequantize, DeltaS, row max): tile 1 starts logits(j) once tile 0 has finished
@@ -763,8 +764,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer (one lane)
-      // QK_t(n) once S_t is free (the softmax read S_t(n-1)) and K(n) has landed; PV_t(n) once
-      // P~_t(n) is written; stage n is released once every MMA reading it has been issued.
+      // QK_t(n) once S_t is free (the softmax read S_t(n-1)), K(n) has landed and PV_t(n-2) has
+      // been issued; PV_t(n) once P~_t(n) is written; stage n is released once every MMA
+      // reading it has been issued.
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
       bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
