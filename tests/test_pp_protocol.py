@@ -1,0 +1,272 @@
+"""CPU model of the two-tile attention kernel's synchronisation (attn_pp in
+bit_exact_attention_gb300/csrc/sage2_attention.cu): producer, event-driven MMA issuer, an
+in-order tensor pipe with commit-to-mbarrier, and the softmax warps of both tiles, all meeting
+on mbarriers that are waited on by phase parity, as the hardware does.
+
+Random interleavings (seeded) are checked for:
+  * parity aliasing: a wait must only pass once the awaited phase has completed, and not when
+    its barrier has run two phases further;
+  * buffer hazards: S_t, the two P~ buffers of each tile, O_t and the K/V stages are only
+    rewritten once every reader of the old contents is done, and only read once written;
+  * deadlock: every run finishes.
+The model follows the kernel's conditions one for one. Two deliberately broken variants (the
+last-tile wait for PV(T-2) removed; QK issued without PV(n-2) issued) must be caught.
+"""
+from __future__ import annotations
+
+import random
+
+import pytest
+
+
+class Hazard(AssertionError):
+    pass
+
+
+class Bar:
+    """mbarrier: `count` arrivals complete a phase; waiters test the phase parity."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.c = name, count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        if self.pending == 0:
+            self.c += 1
+            self.pending = self.count
+
+    def passes(self, n):
+        """Parity test for phase n (what try_wait.parity(n & 1) answers)."""
+        ok = (self.c & 1) != (n & 1)
+        if ok and self.c != n + 1:
+            raise Hazard(f"{self.name}: wait for phase {n} passed with {self.c} completions")
+        return ok
+
+
+class Model:
+    def __init__(self, T0, T1, ST, W, rng, resc_p, last_tile_wait=True, qk_after_pv=True):
+        self.T, self.ST, self.W, self.rng = (T0, T1), ST, W, rng
+        self.Tmax = max(T0, T1)
+        self.resc_p, self.last_tile_wait, self.qk_after_pv = resc_p, last_tile_wait, qk_after_pv
+        B = Bar
+        self.kv_full = [B(f"kv_full{s}", 1) for s in range(ST)]
+        self.kv_empty = [B(f"kv_empty{s}", 1) for s in range(ST)]
+        self.s_full = [B(f"s_full{t}", 1) for t in range(2)]
+        self.s_free = [B(f"s_free{t}", W) for t in range(2)]
+        self.p_full = [[B(f"p_full{t}{b}", W) for b in range(2)] for t in range(2)]
+        self.pv_done = [B(f"pv_done{t}", 1) for t in range(2)]
+        self.tok = [[B(f"tok{t}{w}", 1) for w in range(W)] for t in range(2)]
+        self.pipe = []                       # in-order tensor pipe: MMAs and commits
+        self.stage = [None] * ST             # KV tile held by each stage
+        self.stage_users = {}                # tile -> readers not yet done
+        self.S = [None, None]                # QK index whose result S_t holds
+        self.s_read = [[-1] * W for _ in range(2)]   # last S_t(j) read by each warp
+        self.P = [[[None] * W for _ in range(2)] for _ in range(2)]  # P~ tile in buffer
+        self.pv_completed = [0, 0]
+        self.events = 0                      # steps taken by agents other than the issuer
+
+    # ------------------------------------------------------------ helpers
+    def use_stage(self, n, who):
+        s = n % self.ST
+        if self.stage[s] != n:
+            raise Hazard(f"{who} reads KV tile {n} but stage {s} holds {self.stage[s]}")
+
+    def release_stage_user(self, n, who):
+        self.stage_users[n].discard(who)
+
+    # ------------------------------------------------------------ agents (generators)
+    def producer(self):
+        for j in range(self.Tmax):
+            s = j % self.ST
+            if j >= self.ST:
+                yield ("wait", self.kv_empty[s], j // self.ST - 1)
+                old = j - self.ST
+                if self.stage_users.get(old):
+                    raise Hazard(f"stage {s} reloaded while {sorted(self.stage_users[old])} "
+                                 f"still read KV tile {old}")
+            self.stage[s] = j
+            users = set()
+            for t in range(2):
+                if j < self.T[t]:
+                    users |= {("QK", t), ("PV", t)} | {("SM", t, w) for w in range(self.W)}
+            self.stage_users[j] = users
+            yield ("act", self.kv_full[s].arrive)
+
+    def issuer(self):
+        nq, np_, ne = [0, 0], [0, 0], 0
+        while np_[0] < self.T[0] or np_[1] < self.T[1]:
+            progress = False
+            start = self.events
+            for t in range(2):
+                T = self.T[t]
+                n = np_[t]
+                if n < nq[t] and self.p_full[t][n & 1].passes(n >> 1):
+                    for w in range(self.W):
+                        if self.P[t][n & 1][w] != n:
+                            raise Hazard(f"PV{t}({n}) issued but warp {w}'s P~ buffer holds "
+                                         f"{self.P[t][n & 1][w]}")
+                    self.pipe.append(("PV", t, n))
+                    self.pipe.append(("commit", self.pv_done[t]))
+                    np_[t] += 1
+                    progress = True
+                    while ne < self.Tmax and (ne >= self.T[0] or np_[0] > ne) and \
+                            (ne >= self.T[1] or np_[1] > ne):
+                        self.pipe.append(("commit", self.kv_empty[ne % self.ST]))
+                        ne += 1
+                # the tests are separate instructions: other agents move in between
+                yield ("poll", True)
+                n = nq[t]
+                pv_ok = (np_[t] >= n - 1) if self.qk_after_pv else True
+                if n < T and pv_ok and (n == 0 or self.s_free[t].passes(n - 1)) and \
+                        self.kv_full[n % self.ST].passes(n // self.ST):
+                    if n > 0 and min(self.s_read[t]) < n - 1:
+                        raise Hazard(f"QK{t}({n}) issued before S{t}({n - 1}) was read")
+                    self.pipe.append(("QK", t, n))
+                    self.pipe.append(("commit", self.s_full[t]))
+                    nq[t] += 1
+                    progress = True
+            # idle only if nothing else moved during this pass either
+            yield ("poll", progress or self.events != start)
+
+    def pipe_step(self):
+        kind = self.pipe[0]
+        if kind[0] == "commit":
+            # completes once everything before it has completed: it is at the head
+            self.pipe.pop(0)
+            kind[1].arrive()
+            return
+        if kind[0] == "QK":
+            _, t, n = kind
+            self.use_stage(n, f"QK{t}({n})")
+            self.S[t] = n
+            self.release_stage_user(n, ("QK", t))
+        else:
+            _, t, n = kind
+            self.use_stage(n, f"PV{t}({n})")
+            if self.pv_completed[t] != n:
+                raise Hazard(f"PV{t}({n}) out of order")
+            self.pv_completed[t] += 1
+            self.release_stage_user(n, ("PV", t))
+        self.pipe.pop(0)
+
+    def softmax(self, t, w):
+        T, other = self.T[t], self.T[1 - t]
+        for j in range(T):
+            yield ("wait", self.s_full[t], j)
+            if self.S[t] != j:
+                raise Hazard(f"softmax{t}.{w} reads S{t}({j}) but S holds {self.S[t]}")
+            self.s_read[t][w] = j
+            yield ("act", self.s_free[t].arrive)
+            yield ("wait", self.kv_full[j % self.ST], j // self.ST)
+            if (j >= 1 and j - 1 < other) if t == 0 else (j < other):
+                yield ("wait", self.tok[t][w], j - 1 if t == 0 else j)
+            self.use_stage(j, f"softmax{t}.{w} DeltaS({j})")
+            self.release_stage_user(j, ("SM", t, w))
+            yield ("act", self.tok[1 - t][w].arrive)
+            resc = j > 0 and self.rng.random() < self.resc_p
+            if resc or (self.last_tile_wait and j > 0 and j == T - 1):
+                yield ("wait", self.pv_done[t], j - 1)
+                if resc and self.pv_completed[t] != j:
+                    raise Hazard(f"softmax{t}.{w} rescales O{t} at {j} with "
+                                 f"{self.pv_completed[t]} PVs complete")
+            if self.pv_completed[t] < j - 1:
+                raise Hazard(f"softmax{t}.{w} overwrites P~ buffer {j & 1} before PV{t}({j - 2})")
+            self.P[t][j & 1][w] = j
+            yield ("act", self.p_full[t][j & 1].arrive)
+        if T > 0:
+            yield ("wait", self.pv_done[t], T - 1)
+            if self.pv_completed[t] != T:
+                raise Hazard(f"epilogue{t}.{w} reads O{t} with {self.pv_completed[t]} of {T} PVs")
+
+    # ------------------------------------------------------------ scheduler
+    def run(self, max_steps=200000):
+        agents = {"producer": self.producer(), "issuer": self.issuer()}
+        for t in range(2):
+            for w in range(self.W):
+                agents[f"sm{t}{w}"] = self.softmax(t, w)
+        pending = {k: None for k in agents}  # the action each agent is blocked on
+        idle_issuer = False
+        for _ in range(max_steps):
+            runnable = []
+            for k, req in pending.items():
+                if k not in agents:
+                    continue
+                if req is None:
+                    runnable.append(k)
+                elif req[0] == "wait":
+                    bar, n = req[1], req[2]
+                    if (bar.c & 1) != (n & 1):
+                        runnable.append(k)
+                elif req[0] == "poll":
+                    if not (idle_issuer and not req[1]):
+                        runnable.append(k)
+            if self.pipe:
+                runnable.append("pipe")
+            if not runnable:
+                if not agents:
+                    return
+                if "issuer" in agents and pending["issuer"] and pending["issuer"][0] == "poll":
+                    # the issuer polled without progress and nothing else can move
+                    raise Hazard("deadlock: " + ", ".join(
+                        f"{k}:{pending[k][0]} {getattr(pending[k][1], 'name', '')}"
+                        for k in agents if pending[k]))
+                raise Hazard("deadlock")
+            k = self.rng.choice(runnable)
+            idle_issuer = False
+            if k != "issuer":
+                self.events += 1
+            if k == "pipe":
+                self.pipe_step()
+                continue
+            req = pending[k]
+            if req is not None and req[0] == "wait":
+                req[1].passes(req[2])  # raises on aliasing
+            try:
+                nxt = next(agents[k])
+            except StopIteration:
+                del agents[k]
+                pending[k] = None
+                continue
+            if nxt[0] == "act":
+                nxt[1]()
+                pending[k] = None
+                idle_issuer = False
+            else:
+                pending[k] = nxt
+                if nxt[0] == "poll" and not nxt[1]:
+                    idle_issuer = True
+        raise Hazard("step limit")
+
+
+CASES = [(T0, T1, ST) for (T0, T1) in [(0, 1), (1, 1), (1, 2), (2, 3), (3, 3), (5, 6), (4, 4),
+                                       (0, 3), (6, 2), (9, 10)] for ST in (2, 3, 6)]
+
+
+@pytest.mark.parametrize("T0,T1,ST", CASES)
+def test_two_tile_protocol_has_no_aliasing_hazard_or_deadlock(T0, T1, ST):
+    for seed in range(40):
+        rng = random.Random(seed * 1009 + T0 * 31 + T1 * 7 + ST)
+        Model(T0, T1, ST, W=2, rng=rng, resc_p=rng.choice([0.0, 0.15, 0.5, 1.0])).run()
+
+
+def _caught(**kw):
+    for seed in range(400):
+        rng = random.Random(seed)
+        T0, T1 = rng.choice([(3, 4), (4, 4), (5, 6), (2, 3)])
+        try:
+            Model(T0, T1, 3, W=2, rng=rng, resc_p=0.0, **kw).run()
+        except Hazard:
+            return True
+    return False
+
+
+def test_model_catches_a_missing_last_tile_wait():
+    """Without the wait for PV(T-2) on the last tile, pv_done can lag two phases and the
+    epilogue's parity wait for PV(T-1) passes early: the model must find an interleaving."""
+    assert _caught(last_tile_wait=False)
+
+
+def test_model_catches_qk_issued_before_pv_two_back():
+    """QK(n) before PV(n-2) is issued lets the softmax refill the P~ buffer that PV(n-2) has not
+    read yet (and lets p_full run two phases ahead)."""
+    assert _caught(qk_after_pv=False)
