@@ -54,3 +54,20 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.aggregate_value(2e12, 2.0, 1) == pytest.approx(1.0)
+
+
+def test_traffic_figures_match_their_profiles():
+    """The DRAM bytes that bench.py reports come from the captures summarised under profiles/:
+    the same kernel-source hash and the same counter values, one profile per path."""
+    import re
+
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    files = {"sage2": "traffic_attn_pp_gqa_long_causal_B1_Hq32_Hkv8_N32768_D128.md",
+             "sage1": "traffic_attn_fwd_gqa_long_causal_B1_Hq32_Hkv8_N32768_D128.md"}
+    for (workload, quant), (digest, nbytes) in bench.MEASURED_TRAFFIC.items():
+        text = open(os.path.join(root, "profiles", files[quant])).read()
+        assert f"sha256 prefix `{digest}`" in text, (quant, digest)
+        rows = dict(re.findall(r"\| (dram__bytes_(?:read|write)\.sum) \| ([0-9.]+) MB \|", text))
+        got = (float(rows["dram__bytes_read.sum"]) + float(rows["dram__bytes_write.sum"])) * 1e6
+        assert abs(got - nbytes) <= 0.01e6, (quant, got, nbytes)
