@@ -1,7 +1,9 @@
-"""CPU model of the two-tile attention kernel's synchronisation (attn_pp in
-bit_exact_attention_gb300/csrc/sage2_attention.cu): producer, event-driven MMA issuer, an
-in-order tensor pipe with commit-to-mbarrier, and the softmax warps of both tiles, all meeting
-on mbarriers that are waited on by phase parity, as the hardware does.
+"""CPU models of the attention kernels' synchronisation (bit_exact_attention_gb300/csrc/
+sage2_attention.cu). For attn_pp, the two-tile kernel, the model has a producer, an event-driven
+MMA issuer, an in-order tensor pipe with commit-to-mbarrier, and the softmax warps of both
+tiles. For attn_fwd, the one-tile kernel, it has two issuers with their own pipes, softmax and
+fold warps, a 4-slot alpha ring and double-buffered P~ and R. In both, the agents meet on
+mbarriers that are waited on by phase parity, as the hardware does.
 
 Random interleavings (seeded) are checked for:
   * parity aliasing: a wait must only pass once the awaited phase has completed, and not when
@@ -9,8 +11,11 @@ Random interleavings (seeded) are checked for:
   * buffer hazards: S_t, the two P~ buffers of each tile, O_t and the K/V stages are only
     rewritten once every reader of the old contents is done, and only read once written;
   * deadlock: every run finishes.
-The model follows the kernel's conditions one for one. Two deliberately broken variants (the
-last-tile wait for PV(T-2) removed; QK issued without PV(n-2) issued) must be caught.
+The models follow the kernels' conditions one for one. Each has deliberately broken variants
+that must be caught. For the two-tile kernel these are: the last-tile wait for PV(T-2) removed,
+and QK issued without PV(n-2) issued. For the one-tile kernel: the R-free wait removed, and a
+single-slot alpha ring (a 2-slot ring fails as well, while 3 would do; the kernel keeps 4 for
+mask indexing).
 """
 from __future__ import annotations
 
@@ -270,3 +275,195 @@ def test_model_catches_qk_issued_before_pv_two_back():
     """QK(n) before PV(n-2) is issued lets the softmax refill the P~ buffer that PV(n-2) has not
     read yet (and lets p_full run two phases ahead)."""
     assert _caught(qk_after_pv=False)
+
+
+# ---------------------------------------------------------------------- one-tile kernel
+class OneTileModel:
+    """attn_fwd's protocol: a Q K^T issuer and a P~V issuer (separate threads, so separate
+    in-order pipes whose commits track only their own MMAs), four softmax and four fold warps
+    (modelled with W each), a 4-slot alpha ring, double-buffered P~ and R."""
+
+    def __init__(self, T, ST, W, rng, r_free_wait=True, ring=4):
+        self.T, self.ST, self.W, self.rng, self.r_free_wait, self.ring = T, ST, W, rng, \
+            r_free_wait, ring
+        B = Bar
+        self.q_full = B("q_full", W)
+        self.kv_full = [B(f"kv_full{s}", 1) for s in range(ST)]
+        self.kv_empty = [B(f"kv_empty{s}", 1) for s in range(ST)]
+        self.s_full, self.s_free = B("s_full", 1), B("s_free", W)
+        self.p_full = [B(f"p_full{b}", W) for b in range(2)]
+        self.pv_done = [B(f"pv_done{b}", 1) for b in range(2)]
+        self.r_free = [B(f"r_free{b}", W) for b in range(2)]
+        self.a_full = [B(f"a_full{s}", W) for s in range(ring)]
+        self.l_full = B("l_full", W)
+        self.pipes = {"qk": [], "pv": []}
+        self.stage, self.stage_users = [None] * ST, {}
+        self.S, self.s_read = None, [-1] * W
+        self.P = [[None] * W for _ in range(2)]
+        self.R = [None, None]
+        self.r_read = [[-1] * W for _ in range(2)]
+        self.alpha = [[None] * W for _ in range(ring)]
+        self.pv_completed = 0
+        self.qk_completed = 0
+        self.folded = [-1] * W
+
+    def use_stage(self, n, who):
+        if self.stage[n % self.ST] != n:
+            raise Hazard(f"{who} reads KV tile {n} but its stage holds {self.stage[n % self.ST]}")
+
+    def producer(self):
+        for j in range(self.T):
+            s = j % self.ST
+            if j >= self.ST:
+                yield ("wait", self.kv_empty[s], j // self.ST - 1)
+                if self.stage_users.get(j - self.ST):
+                    raise Hazard(f"stage {s} reloaded while {sorted(self.stage_users[j - self.ST])}"
+                                 f" still read KV tile {j - self.ST}")
+            self.stage[s] = j
+            self.stage_users[j] = {"QK", "PV"} | {("SM", w) for w in range(self.W)}
+            yield ("act", self.kv_full[s].arrive)
+
+    def qk_issuer(self):
+        yield ("wait", self.q_full, 0)
+        for j in range(self.T):
+            if j:
+                yield ("wait", self.s_free, j - 1)
+                if min(self.s_read) < j - 1:
+                    raise Hazard(f"QK({j}) issued before S({j - 1}) was read")
+            yield ("wait", self.kv_full[j % self.ST], j // self.ST)
+            self.pipes["qk"] += [("QK", j), ("commit", self.s_full)]
+
+    def pv_issuer(self):
+        for j in range(self.T):
+            b = j & 1
+            yield ("wait", self.p_full[b], j >> 1)
+            if j >= 2 and self.r_free_wait:
+                yield ("wait", self.r_free[b], (j - 2) >> 1)
+            if any(p != j for p in self.P[b]):
+                raise Hazard(f"PV({j}) issued but the P~ buffer holds {self.P[b]}")
+            if self.qk_completed <= j:
+                raise Hazard(f"stage of KV tile {j} released before QK({j}) completed")
+            self.pipes["pv"] += [("PV", j), ("commit", self.pv_done[b]),
+                                 ("commit", self.kv_empty[j % self.ST])]
+
+    def pipe_step(self, name):
+        head = self.pipes[name].pop(0)
+        if head[0] == "commit":
+            head[1].arrive()
+            return
+        j = head[1]
+        self.use_stage(j, f"{head[0]}({j})")
+        if head[0] == "QK":
+            self.S = j
+            self.qk_completed = j + 1
+            self.stage_users[j].discard("QK")
+        else:
+            b = j & 1
+            if j >= 2 and min(self.r_read[b]) < j - 2:
+                raise Hazard(f"PV({j}) overwrites R{b} before the fold read R({j - 2})")
+            self.R[b] = j
+            self.pv_completed = j + 1
+            self.stage_users[j].discard("PV")
+
+    def softmax(self, w):
+        yield ("act", self.q_full.arrive)
+        jprev = None
+
+        def hand_over(n):
+            slot = n % self.ring
+            if n >= self.ring and self.folded[w] < n - self.ring:
+                raise Hazard(f"alpha({n}) overwrites slot {slot} before the fold read "
+                             f"alpha({n - self.ring})")
+            self.alpha[slot][w] = n
+
+        for j in range(self.T):
+            yield ("wait", self.s_full, j)
+            if self.S != j:
+                raise Hazard(f"softmax {w} reads S({j}) but S holds {self.S}")
+            self.s_read[w] = j
+            yield ("act", self.s_free.arrive)
+            if jprev is not None:
+                hand_over(jprev)
+                yield ("act", self.p_full[jprev & 1].arrive)
+                yield ("act", self.a_full[jprev % self.ring].arrive)
+            yield ("wait", self.kv_full[j % self.ST], j // self.ST)
+            if j >= 2:
+                yield ("wait", self.pv_done[j & 1], (j - 2) >> 1)
+            self.use_stage(j, f"softmax {w} DeltaS({j})")
+            self.stage_users[j].discard(("SM", w))
+            if self.pv_completed < j - 1:
+                raise Hazard(f"softmax {w} overwrites P~ buffer {j & 1} before PV({j - 2})")
+            self.P[j & 1][w] = j
+            jprev = j
+        if jprev is not None:
+            hand_over(jprev)
+            yield ("act", self.p_full[jprev & 1].arrive)
+            yield ("act", self.a_full[jprev % self.ring].arrive)
+        yield ("act", self.l_full.arrive)
+
+    def fold(self, w):
+        for j in range(self.T):
+            yield ("wait", self.a_full[j % self.ring], j // self.ring)
+            if self.alpha[j % self.ring][w] != j:
+                raise Hazard(f"fold {w} reads alpha({j}) but the slot holds "
+                             f"{self.alpha[j % self.ring][w]}")
+            self.folded[w] = j
+            yield ("wait", self.pv_done[j & 1], j >> 1)
+            if self.R[j & 1] != j:
+                raise Hazard(f"fold {w} reads R({j}) but R{j & 1} holds {self.R[j & 1]}")
+            self.r_read[j & 1][w] = j
+            yield ("act", self.r_free[j & 1].arrive)
+        yield ("wait", self.l_full, 0)
+        if self.pv_completed != self.T:
+            raise Hazard("epilogue before every PV completed")
+
+    def run(self, max_steps=200000):
+        agents = {"producer": self.producer(), "qk": self.qk_issuer(), "pv": self.pv_issuer()}
+        for w in range(self.W):
+            agents[f"sm{w}"] = self.softmax(w)
+            agents[f"fold{w}"] = self.fold(w)
+        pending = {k: None for k in agents}
+        for _ in range(max_steps):
+            choices = [k for k in agents if pending[k] is None or
+                       (pending[k][1].c & 1) != (pending[k][2] & 1)]
+            choices += [("pipe", p) for p in ("qk", "pv") if self.pipes[p]]
+            if not choices:
+                if agents:
+                    raise Hazard("deadlock: " + ", ".join(
+                        f"{k}:{pending[k][1].name}" for k in agents if pending[k]))
+                return
+            k = self.rng.choice(choices)
+            if isinstance(k, tuple):
+                self.pipe_step(k[1])
+                continue
+            if pending[k] is not None:
+                pending[k][1].passes(pending[k][2])  # raises on aliasing
+            try:
+                nxt = next(agents[k])
+            except StopIteration:
+                del agents[k]
+                continue
+            if nxt[0] == "act":
+                nxt[1]()
+                pending[k] = None
+            else:
+                pending[k] = nxt
+        raise Hazard("step limit")
+
+
+@pytest.mark.parametrize("T,ST", [(T, ST) for T in (1, 2, 3, 5, 8, 13) for ST in (2, 4, 6)])
+def test_one_tile_protocol_has_no_aliasing_hazard_or_deadlock(T, ST):
+    for seed in range(40):
+        OneTileModel(T, ST, W=2, rng=random.Random(seed * 131 + T * 7 + ST)).run()
+
+
+def test_one_tile_model_catches_a_missing_r_free_wait_and_a_short_alpha_ring():
+    def caught(**kw):
+        for seed in range(300):
+            try:
+                OneTileModel(8, 4, W=2, rng=random.Random(seed), **kw).run()
+            except Hazard:
+                return True
+        return False
+    assert caught(r_free_wait=False)
+    assert caught(ring=1)
