@@ -90,7 +90,7 @@ constexpr uint32_t kTmemCols = 512;
 enum : int {
   kSiteQ = 1, kSiteKvFull = 2, kSiteKvEmpty = 3, kSiteSFull = 4, kSitePFull = 5, kSiteRFull = 6,
   kSiteRFree = 7, kSiteKvFullSm = 8, kSiteAFull = 9, kSiteLFull = 10, kSiteSFree = 11,
-  kSitePvDone = 12, kSiteTok = 13
+  kSitePvDone = 12
 };
 
 struct AttnArgs {
@@ -168,6 +168,65 @@ __device__ __forceinline__ float logits64(float (&x)[64], const uint32_t (&v)[64
 #pragma unroll
     for (int k = 0; k < 4; ++k) mk[k] = max3(mk[k], x[16 * k + e], x[16 * k + e + 1]);
   return max3(mk[0], mk[1], fmaxf(mk[2], mk[3]));
+}
+
+// The logits of one 128-key tile of a softmax row, on packed FP32 pairs (key 2k in x[k].x, key
+// 2k + 1 in x[k].y): S' = fma(A, fl32(sqc * s_K), DeltaS c), one K scale per 32 keys, -inf
+// beyond key `lim`; returns the row maximum of the tile.
+__device__ __forceinline__ float logits128(float2 (&x)[64], const uint32_t (&v)[128],
+                                           const float *dsc, const float *skv, float sqc, int lim) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float mult = __fmul_rn(sqc, skv[c]);
+    const float2 m2 = make_float2(mult, mult);
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 d4 = *reinterpret_cast<const float4 *>(dsc + c * 32 + e);
+      const int k = (c * 32 + e) >> 1;
+      x[k] = __ffma2_rn(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), m2,
+                        make_float2(d4.x, d4.y));
+      x[k + 1] =
+          __ffma2_rn(make_float2(__uint_as_float(v[2 * k + 2]), __uint_as_float(v[2 * k + 3])), m2,
+                     make_float2(d4.z, d4.w));
+    }
+  }
+  if (lim < 127) {  // diagonal / ragged tile: keys beyond lim are not visible
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+      x[k].x = (2 * k <= lim) ? x[k].x : -INFINITY;
+      x[k].y = (2 * k + 1 <= lim) ? x[k].y : -INFINITY;
+    }
+  }
+  float mk[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) mk[q] = fmaxf(x[q].x, x[q].y);
+#pragma unroll
+  for (int k = 4; k < 64; ++k) mk[k & 3] = max3(mk[k & 3], x[k].x, x[k].y);
+  return max3(mk[0], mk[1], fmaxf(mk[2], mk[3]));
+}
+
+// P448 = 2^(S' - m448) for the 128 keys of a row (masked keys give 0), their sum (pairs summed
+// into four accumulators by pair index mod 4, then combined in a fixed order) and the e4m3 codes
+// P~ = e4m3(P448), key 4e + i in byte i of pk[e].
+__device__ __forceinline__ float probs128(float2 (&x)[64], float m448, uint32_t (&pk)[32]) {
+  const float2 nm = make_float2(-m448, -m448);
+#pragma unroll
+  for (int k = 0; k < 64; ++k) {
+    x[k] = __fadd2_rn(x[k], nm);
+    x[k].x = ex2_approx(x[k].x);
+    x[k].y = ex2_approx(x[k].y);
+  }
+  float2 ps[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) ps[q] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < 64; ++k) ps[k & 3] = __fadd2_rn(ps[k & 3], x[k]);
+  const float rs = __fadd_rn(__fadd_rn(__fadd_rn(ps[0].x, ps[0].y), __fadd_rn(ps[1].x, ps[1].y)),
+                             __fadd_rn(__fadd_rn(ps[2].x, ps[2].y), __fadd_rn(ps[3].x, ps[3].y)));
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    pk[e] = cvt_e4m3x4(x[2 * e].x, x[2 * e].y, x[2 * e + 1].x, x[2 * e + 1].y);
+  return rs;
 }
 
 // End of every role branch: all 512 threads meet once more (each warp from its own branch, so
@@ -590,24 +649,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------- two-tile (ping-pong) kernel
+// ---------------------------------------------------------------- two-tile kernel
 // One CTA per (sequence, q head, pair of 128-row Q tiles); the two tiles share every K/V stage,
-// so each K/V byte brought in feeds twice the tensor work. Warps: 0 TMA producer, 1 MMA issuer,
-// 2 idle, 3 stages the V channel scales, 4-7 softmax + epilogue of tile 0, 8-11 of tile 1 (each
-// SM sub-partition runs one softmax warp of each tile, so one tile's arithmetic fills the
-// other's MMA latency).
+// so each K/V byte brought in feeds twice the tensor work. Warps: 0 TMA producer, 1 Q K^T issuer,
+// 2 P~V issuer, 3 stages the V channel scales, 4-7 softmax + epilogue of tile 0, 8-11 of tile 1
+// (each SM sub-partition runs one softmax warp of each tile, so one tile's arithmetic fills the
+// other's waits).
 // Per tile t: tensor memory S_t [256 t, 256 t + 128) and O_t [256 t + 128, 256 t + 128 + DP) (the
 // FP32 output accumulator); Q_t codes and two P~_t buffers (128 x 128 e4m3, the A operand of
 // P~V) in shared memory, 128-byte swizzled K-major. Per KV tile j the softmax loads S_t(j) into
-// registers and releases S_t at once (QK_t(j+1) may start) and computes P~_t(j). If a row maximum
-// of the warp moved, it waits for PV_t(j-1) and rescales O_t by alpha(j). It writes P~_t(j) into
-// buffer j % 2 and hands it to the issuer; PV_t(j) then adds the block partial P~(j) V(j) into
-// O_t.
-// The issuer is event driven: it issues whichever of QK_0, PV_0, QK_1, PV_1 is ready.
-// The softmax warps of the two tiles that share a sub-partition take turns on the logits phase
-// (ALU bound: dequantize, DeltaS, row max): tile 1 starts logits(j) once tile 0 has finished
-// logits(j), tile 0 starts logits(j+1) once tile 1 has finished logits(j). So one warp's
-// exponentials (MUFU bound) overlap the other's logits instead of both warps doing the same phase.
+// registers and releases S_t at once, so QK_t(j+1) runs while it computes P~_t(j). If a row
+// maximum of the warp moved, it waits for PV_t(j-1) and rescales O_t by alpha(j) in tensor memory.
+// It writes P~_t(j) into buffer j % 2 (free: QK_t(j) is issued only after PV_t(j-2) completed)
+// and hands it to the P~V issuer; PV_t(j) then adds the block partial P~(j) V(j) into O_t.
+// The two issuers are event driven and independent of each other. Issuing a group of MMAs blocks
+// the issuing thread while the tensor pipe is busy (a few hundred cycles per group); with one
+// thread for both products, each P~V issue delayed the next Q K^T of both tiles by that much, and
+// the softmax waited for S. tcgen05.commit covers the MMAs of the issuing thread only, so each
+// issuer signals its own products: s_full_t after QK_t(n), pv_done[t][n % 2] after PV_t(n), and
+// one arrival each on a stage's empty barrier once all its products reading the stage are issued.
 template <int DP, int ST>
 struct PPPlan {
   static constexpr int kQ = 0;                       // [2][128 rows][DP]   (swizzled)
@@ -618,20 +678,88 @@ struct PPPlan {
   static constexpr int kSk = kDsc + ST * 2 * 512;    // float [ST][4]
   static constexpr int kSv = kSk + ST * 16;          // float [DP]
   static constexpr int kBar = kSv + DP * 4;
-  // q, full[ST], empty[ST], s_full[2], s_free[2], p_full[2][2], pv_done[2], drain, tok[2][4]
-  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 4 + 2 + 1 + 8;
+  // q, full[ST], empty[ST], s_full[2], s_free[2], p_full[2][2], pv_done[2][2], drain[2]
+  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 4 + 4 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kBytes = kEnd + 1024;
   static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
-// register split: the control warpgroup keeps 56 (its event loop spills at 40), the two softmax
+// register split: the control warpgroup keeps 56 (its event loops spill at 40), the two softmax
 // warpgroups take 224 each (56 + 2 x 224 = 3 x 168, the launch budget)
 constexpr int kPPRegsCtl = 56, kPPRegsSoftmax = 224;
 static_assert(kPPRegsCtl + 2 * kPPRegsSoftmax <= 3 * kRegsLaunch, "register split above budget");
+static_assert(kPvWarp != 3, "warp 3 stages the V channel scales");
 // tensor-memory columns of tile t: S at 256 t, O at 256 t + 128
 __device__ __forceinline__ uint32_t pp_col_s(int t) { return (uint32_t)t * 256u; }
 __device__ __forceinline__ uint32_t pp_col_o(int t) { return (uint32_t)t * 256u + 128u; }
+
+// Idle bookkeeping of an event-driven issuer: after SAGE2_WAIT_NS of global time without
+// progress (or once another warp gave up) it gives up too, recording `site`.
+struct IdleClock {
+  uint64_t t_idle = 0;  // global time when the current idle spell was first checked
+  uint32_t idle = 0;    // polls without progress (the clock is read every 64th)
+  __device__ __forceinline__ bool step(bool progress, const AbortCtx &ab, int site) {
+    if (progress) {
+      idle = 0;
+      return true;
+    }
+    if ((++idle & 63u) != 0) return true;
+    const uint64_t now = global_timer_ns();
+    if (idle == 64) t_idle = now;
+    if (*ab.flag) return false;
+    if (now - t_idle > SAGE2_WAIT_NS) {
+      *ab.flag = 1;
+      if (ab.status) atomicCAS(ab.status, 0, kStatusTimeoutBase | site);
+      return false;
+    }
+    return true;
+  }
+};
+
+// One 128-row tile's output rows from the FP32 accumulator in tensor memory: O * vscale / l,
+// rounded to the output type (row `row` of the tile, `o` its element offset in the output).
+template <int DP>
+__device__ __forceinline__ void store_out_row(const AttnArgs &a, uint32_t tO, const float *sv_s,
+                                              float l, bool row_ok, size_t o) {
+  const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
+#pragma unroll
+  for (int c = 0; c < DP / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32_wait(tO + 32 * c, r);
+#pragma unroll
+    for (int e8 = 0; e8 < 32; e8 += 8) {
+      const int d = 32 * c + e8;
+      if (row_ok && d < a.g.D0) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          y[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[e8 + e]), sv_s[d + e]), inv_l);
+        if (a.out_dtype == SAGE2_FP32) {
+          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + o + d);
+          dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+          dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+        } else {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint16_t lo, hi;
+            if (a.out_dtype == SAGE2_BF16) {
+              lo = __bfloat16_as_ushort(__float2bfloat16_rn(y[2 * e]));
+              hi = __bfloat16_as_ushort(__float2bfloat16_rn(y[2 * e + 1]));
+            } else {
+              lo = __half_as_ushort(__float2half_rn(y[2 * e]));
+              hi = __half_as_ushort(__float2half_rn(y[2 * e + 1]));
+            }
+            w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+          }
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + o + d) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  }
+}
 
 // DBG: one CTA, the pair holding Q tile a.dbg.qt of (sequence a.dbg.b, head a.dbg.h); the
 // softmax warps of that tile dump S(kt) (the raw integer accumulators) and P~(kt), and for
@@ -682,13 +810,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::kBar);
   uint64_t *q_full = bars;
   uint64_t *kv_full = bars + 1;
-  uint64_t *kv_empty = kv_full + ST;
-  uint64_t *s_full = kv_empty + ST;  // [2] QK_t(j) complete
-  uint64_t *s_free = s_full + 2;     // [2] the softmax of tile t has read S_t(j)
-  uint64_t *p_full = s_free + 2;     // [2][2] P~_t(j) written into buffer j % 2, O_t rescaled
-  uint64_t *pv_done = p_full + 4;    // [2] PV_t(j) complete
-  uint64_t *drain = pv_done + 2;
-  uint64_t *tok = drain + 1;         // [2][4] tok[t][w]: the other tile's warp w finished logits
+  uint64_t *kv_empty = kv_full + ST;  // one arrival from each issuer
+  uint64_t *s_full = kv_empty + ST;   // [2] QK_t(j) complete
+  uint64_t *s_free = s_full + 2;      // [2] the softmax of tile t has read S_t(j)
+  uint64_t *p_full = s_free + 2;      // [2][2] P~_t(j) written into buffer j % 2, O_t rescaled
+  uint64_t *pv_done = p_full + 4;     // [2][2] PV_t(n) complete, by n % 2
+  uint64_t *drain = pv_done + 4;      // [2] one per issuer
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kMisc + 4);
   float *sv_s = reinterpret_cast<float *>(smem + P::kSv);
@@ -697,17 +824,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < ST; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&s_free[t], 4);
-      mbar_init(&p_full[2 * t], 4);
-      mbar_init(&p_full[2 * t + 1], 4);
-      mbar_init(&pv_done[t], 1);
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&p_full[2 * t + k], 4);
+        mbar_init(&pv_done[2 * t + k], 1);
+      }
     }
-    mbar_init(drain, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&tok[i], 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_q);
@@ -727,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const AbortCtx ab{abort_flag, a.status};
+  const int T0 = Tt[0], T1 = Tt[1];
 
   if (warp < 4) {
     regs_release<kPPRegsCtl>();
@@ -745,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < Tmax; ++j) {
         const int st = j % ST;
         if (j >= ST && !mbar_wait<true>(&kv_empty[st], ((j / ST) - 1) & 1, ab, kSiteKvEmpty)) break;
-        const bool u0 = j < Tt[0], u1 = j < Tt[1];
+        const bool u0 = j < T0, u1 = j < T1;
         mbar_arrive_expect_tx(&kv_full[st],
                               128 * DP + DP * 128 + ((u0 ? 1 : 0) + (u1 ? 1 : 0)) * 512 + 16);
         tma_load_2d(smem + P::kK + st * 128 * DP, &tm_k, 0, yk0 + j * kBKV, &kv_full[st]);
@@ -763,46 +892,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(q_full, 0);
       }
     } else if (warp == kMmaWarp && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer (one lane)
-      // QK_t(n) once S_t is free (the softmax read S_t(n-1)), K(n) has landed and PV_t(n-2) has
-      // been issued; PV_t(n) once P~_t(n) is written; stage n is released once every MMA
-      // reading it has been issued.
+      // ---------------------------------------------------------- Q K^T issuer (one lane)
+      // QK_t(n) once K(n) has landed, the softmax of tile t has read S_t(n-1) and PV_t(n-2) is
+      // complete: the softmax then knows from s_full_t(n) alone that P~ buffer n % 2 is free. This
+      // thread tests every phase of pv_done[t][b] in order, so the softmax's own parity waits on
+      // those barriers (PV_t(j-1) for a rescale, PV_t(T-1) for the epilogue) come at most one
+      // phase ahead of what has been seen complete. Stage n is released (this issuer's arrival)
+      // once QK_0(n) and QK_1(n) have been issued.
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
-      constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
       bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
-      int nq0 = 0, nq1 = 0, np0 = 0, np1 = 0, ne = 0;
-      const int T0 = Tt[0], T1 = Tt[1];
-      uint64_t t_idle = 0;  // global time when the current idle spell was first checked
-      uint32_t idle = 0;    // polls without progress (the clock is read every 64th)
-      while (ok && (np0 < T0 || np1 < T1)) {
+      int nq0 = 0, nq1 = 0, ne = 0;
+      IdleClock clk;
+      while (ok && (nq0 < T0 || nq1 < T1)) {
         bool progress = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           int &nq = t ? nq1 : nq0;
-          int &np = t ? np1 : np0;
           const int T = t ? T1 : T0;
-          if (np < nq && mbar_test_wait(&p_full[2 * t + (np & 1)], (np >> 1) & 1)) {
-            tc_fence_after();
-            const uint64_t pdesc =
-                sdesc_kmajor(smem_u32(smem + P::kP + (2 * t + (np & 1)) * 16384), 128);
-            const uint64_t vdesc =
-                sdesc_kmajor(smem_u32(smem + P::kV + (np % ST) * DP * 128), 128);
-#pragma unroll
-            for (int kk = 0; kk < kBKV / 32; ++kk)
-              mma_e4m3_ss(tbase + pp_col_o(t), pdesc + (uint64_t)(kk * 2),
-                          vdesc + (uint64_t)(kk * 2), idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&pv_done[t]);
-            ++np;
-            progress = true;
-            // release every stage whose MMAs have all been issued
-            while (ne < Tmax && (ne >= T0 || np0 > ne) && (ne >= T1 || np1 > ne)) {
-              mma_commit(&kv_empty[ne % ST]);
-              ++ne;
-            }
-          }
-          // QK_t(nq) after PV_t(nq-2): its commit then also covers PV_t(nq-2), which frees the
-          // P~ buffer that the softmax of tile nq refills
-          if (nq < T && np >= nq - 1 && (nq == 0 || mbar_test_wait(&s_free[t], (nq - 1) & 1)) &&
+          if (nq < T && (nq == 0 || mbar_test_wait(&s_free[t], (nq - 1) & 1)) &&
+              (nq < 2 || mbar_test_wait(&pv_done[2 * t + (nq & 1)], ((nq - 2) >> 1) & 1)) &&
               mbar_test_wait(&kv_full[nq % ST], (nq / ST) & 1)) {
             tc_fence_after();
             const uint64_t adesc = sdesc_kmajor(smem_u32(smem + P::kQ + t * 128 * DP), DP);
@@ -815,24 +923,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&s_full[t]);
             ++nq;
             progress = true;
+            while (ne < Tmax && (ne >= T0 || nq0 > ne) && (ne >= T1 || nq1 > ne)) {
+              mma_commit(&kv_empty[ne % ST]);
+              ++ne;
+            }
           }
         }
-        if (progress) {
-          idle = 0;
-        } else if ((++idle & 63u) == 0) {
-          const uint64_t now = global_timer_ns();
-          if (idle == 64) t_idle = now;
-          if (*abort_flag) {
-            ok = false;
-          } else if (now - t_idle > SAGE2_WAIT_NS) {
-            *abort_flag = 1;
-            atomicCAS(a.status, 0, kStatusTimeoutBase | kSitePFull);
-            ok = false;
-          }
-        }
+        ok = clk.step(progress, ab, kSiteSFree);
       }
-      mma_commit(drain);  // every MMA issued above completes before tensor memory is freed
-      drain_wait(drain, 0);
+      mma_commit(&drain[0]);  // every MMA issued above completes before tensor memory is freed
+      drain_wait(&drain[0], 0);
+    } else if (warp == kPvWarp && lane == 0) {
+      // ---------------------------------------------------------- P~V issuer (one lane)
+      // PV_t(n) once P~_t(n) is written (after the rescale of O_t); stage n is released (this
+      // issuer's arrival) once PV_0(n) and PV_1(n) have been issued. The kv_full test is already
+      // complete when P~_t(n) exists (QK_t(n) waited for it); it orders the V reads after the
+      // copy for this thread too.
+      constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
+      bool ok = true;
+      int np0 = 0, np1 = 0, ne = 0;
+      IdleClock clk;
+      while (ok && (np0 < T0 || np1 < T1)) {
+        bool progress = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          int &np = t ? np1 : np0;
+          const int T = t ? T1 : T0;
+          if (np < T && mbar_test_wait(&p_full[2 * t + (np & 1)], (np >> 1) & 1) &&
+              mbar_test_wait(&kv_full[np % ST], (np / ST) & 1)) {
+            tc_fence_after();
+            const uint64_t pdesc =
+                sdesc_kmajor(smem_u32(smem + P::kP + (2 * t + (np & 1)) * 16384), 128);
+            const uint64_t vdesc =
+                sdesc_kmajor(smem_u32(smem + P::kV + (np % ST) * DP * 128), 128);
+#pragma unroll
+            for (int kk = 0; kk < kBKV / 32; ++kk)
+              mma_e4m3_ss(tbase + pp_col_o(t), pdesc + (uint64_t)(kk * 2),
+                          vdesc + (uint64_t)(kk * 2), idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&pv_done[2 * t + (np & 1)]);
+            ++np;
+            progress = true;
+            while (ne < Tmax && (ne >= T0 || np0 > ne) && (ne >= T1 || np1 > ne)) {
+              mma_commit(&kv_empty[ne % ST]);
+              ++ne;
+            }
+          }
+        }
+        ok = clk.step(progress, ab, kSitePFull);
+      }
+      mma_commit(&drain[1]);
+      drain_wait(&drain[1], 0);
     }
     cta_teardown(warp == kMmaWarp, tbase);
   } else {
@@ -877,7 +1017,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t v[128];
         tmem_ld128_nowait(tS, v);
-        const bool kv_ready = mbar_try_wait(&kv_full[st], (j / ST) & 1);
         tmem_wait_ld128(v);  // S_t(j) is in registers: QK_t(j+1) may overwrite S_t
         const bool dump = DBG && t == (a.dbg.qt & 1) && j == a.dbg.kt;
         if (dump) {
@@ -887,92 +1026,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[t]);
-        ok = warp_all(kv_ready || mbar_wait(&kv_full[st], (j / ST) & 1, ab, kSiteKvFullSm));
-        if (!ok) break;
-        // my turn for the logits phase (S is already loaded and released): tile 0 waits for
-        // tile 1's logits(j-1), tile 1 for tile 0's logits(j) (only while the other tile still
-        // has those tiles)
-        if (t == 0 ? (j >= 1 && j - 1 < Tt[1]) : (j < Tt[0])) {
-          ok = warp_all(mbar_wait(&tok[t * 4 + qd], (t == 0 ? j - 1 : j) & 1, ab, kSiteTok));
-          if (!ok) break;
-        }
+        // DeltaS*c and the K scales of stage st: the copy completed kv_full(j), which the Q K^T
+        // issuer waited for before issuing QK_t(j), whose completion (s_full) this warp has seen
         const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 1024 + t * 512);
         const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
         const int lim = last_key - j * kBKV;
-        float x[128];
-        float pmax = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float xh[64];
-          uint32_t vh[64];
-#pragma unroll
-          for (int e = 0; e < 64; ++e) vh[e] = v[64 * h + e];
-          pmax = fmaxf(pmax, logits64<true>(xh, vh, dsc + 64 * h, skv + 2 * h, sqc, lim - 64 * h));
-#pragma unroll
-          for (int e = 0; e < 64; ++e) x[64 * h + e] = xh[e];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tok[(1 - t) * 4 + qd]);  // the other tile's turn
+        float2 x[64];
+        const float pmax = logits128(x, v, dsc, skv, sqc, lim);
         const float m_new = fmaxf(m, pmax);
         const bool none = (m_new == -INFINITY);
         const float alpha = none ? 1.f : ex2_approx(__fsub_rn(m, m_new));
         const float m448 = none ? 0.f : __fsub_rn(m_new, L32);
-#pragma unroll
-        for (int e = 0; e < 128; e += 2) add2(x[e], x[e + 1], x[e], x[e + 1], -m448, -m448);
-#pragma unroll
-        for (int e = 0; e < 128; ++e) x[e] = ex2_approx(x[e]);
-        float ps[4][2];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ps[k][0] = ps[k][1] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 128; e += 2)
-          add2(ps[(e >> 1) & 3][0], ps[(e >> 1) & 3][1], ps[(e >> 1) & 3][0], ps[(e >> 1) & 3][1],
-               x[e], x[e + 1]);
-        const float rs = __fadd_rn(
-            __fadd_rn(__fadd_rn(ps[0][0], ps[0][1]), __fadd_rn(ps[1][0], ps[1][1])),
-            __fadd_rn(__fadd_rn(ps[2][0], ps[2][1]), __fadd_rn(ps[3][0], ps[3][1])));
         uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          pk[e] = cvt_e4m3x2(x[4 * e], x[4 * e + 1]) | (cvt_e4m3x2(x[4 * e + 2], x[4 * e + 3]) << 16);
+        const float rs = probs128(x, m448, pk);
         if (dump) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             *reinterpret_cast<uint32_t *>(a.dbg.p_out + row * 128 + 4 * e) = pk[e];
         }
-        // O = alpha O once PV_t(j-1) has added its partial; with every alpha of the warp's rows
-        // equal to 1 there is nothing to wait for, except on the last tile: pv_done_t may then
-        // lag two phases behind (only QK_t(j) complete implies PV_t(j-2)), and the wait for
-        // PV_t(j-1) here keeps the epilogue's parity wait for PV_t(T-1) unambiguous
-        const bool resc = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-        if (resc || (j > 0 && j == T - 1)) {
-          ok = warp_all(mbar_wait(&pv_done[t], (j - 1) & 1, ab, kSitePvDone));
+        // O = alpha O once PV_t(j-1) is complete (with every alpha of the warp's rows equal to 1
+        // there is nothing to do). P~ buffer j % 2 is free: QK_t(j) was issued after PV_t(j-2)
+        // had completed.
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          ok = warp_all(
+              mbar_wait(&pv_done[2 * t + ((j - 1) & 1)], ((j - 1) >> 1) & 1, ab, kSitePvDone));
           if (!ok) break;
           tc_fence_after();
-          if (resc) {
 #pragma unroll
-            for (int h = 0; h < DP / 64; ++h) {  // 64 columns per load
-              uint32_t ov[64];
-              tmem_ld64(tO + 64 * h, ov);
+          for (int h = 0; h < DP / 64; ++h) {  // 64 columns per load
+            uint32_t ov[64];
+            tmem_ld64(tO + 64 * h, ov);
 #pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                uint32_t r[32];
+            for (int c = 0; c < 2; ++c) {
+              uint32_t r[32];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                  float y0, y1;
-                  mul2(y0, y1, __uint_as_float(ov[32 * c + e]), __uint_as_float(ov[32 * c + e + 1]),
-                       alpha, alpha);
-                  r[e] = __float_as_uint(y0);
-                  r[e + 1] = __float_as_uint(y1);
-                }
-                tmem_st32(tO + 64 * h + 32 * c, r);
+              for (int e = 0; e < 32; e += 2) {
+                const float2 y = __fmul2_rn(
+                    make_float2(__uint_as_float(ov[32 * c + e]), __uint_as_float(ov[32 * c + e + 1])),
+                    make_float2(alpha, alpha));
+                r[e] = __float_as_uint(y.x);
+                r[e + 1] = __float_as_uint(y.y);
               }
+              tmem_st32(tO + 64 * h + 32 * c, r);
             }
-            tmem_st_wait();
           }
+          tmem_st_wait();
         }
-        // buffer j % 2 is free: PV_t(j-2) was issued before QK_t(j), whose completion (s_full)
-        // implies it
         uint8_t *prow = prow0 + (j & 1) * 16384;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -983,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[2 * t + (j & 1)]);
         if (dump && j == 0) {  // O after PV(0) is the fresh partial P~(0) V(0)
-          ok = warp_all(mbar_wait(&pv_done[t], 0, ab, kSitePvDone));
+          ok = warp_all(mbar_wait(&pv_done[2 * t], 0, ab, kSitePvDone));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -998,46 +1097,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       }
       // ---------------------------------------------------------- epilogue
-      if (ok) ok = warp_all(mbar_wait(&pv_done[t], (T - 1) & 1, ab, kSitePvDone));
+      // PV_t(T-1) on its buffer's barrier, whose previous phase (PV_t(T-3)) the Q K^T issuer saw
+      // complete before issuing QK_t(T-1)
+      if (ok)
+        ok = warp_all(
+            mbar_wait(&pv_done[2 * t + ((T - 1) & 1)], ((T - 1) >> 1) & 1, ab, kSitePvDone));
       if (warp_all(ok && !*abort_flag)) {
         tc_fence_after();
-        const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
-#pragma unroll
-        for (int c = 0; c < DP / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32_wait(tO + 32 * c, r);
-#pragma unroll
-          for (int e8 = 0; e8 < 32; e8 += 8) {
-            const int d = 32 * c + e8;
-            if (row_ok && d < g.D0) {
-              float y[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                y[e] = __fmul_rn(__fmul_rn(__uint_as_float(r[e8 + e]), sv_s[d + e]), inv_l);
-              if (a.out_dtype == SAGE2_FP32) {
-                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + o + d);
-                dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-                dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-              } else {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  uint16_t lo, hi;
-                  if (a.out_dtype == SAGE2_BF16) {
-                    lo = __bfloat16_as_ushort(__float2bfloat16_rn(y[2 * e]));
-                    hi = __bfloat16_as_ushort(__float2bfloat16_rn(y[2 * e + 1]));
-                  } else {
-                    lo = __half_as_ushort(__float2half_rn(y[2 * e]));
-                    hi = __half_as_ushort(__float2half_rn(y[2 * e + 1]));
-                  }
-                  w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-                }
-                *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + o + d) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          }
-        }
+        store_out_row<DP>(a, tO, sv_s, l, row_ok, o);
       }
     }
     cta_teardown(false, tbase);
@@ -1155,11 +1222,11 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
     CUtensorMap mq;
     if (!make_map(&mq, w.qcode, g.Dp, (uint64_t)g.Hq * L.Tq, g.Dp, 128, qk_sw))
       return cudaErrorInvalidValue;
+    const dim3 grid2((nqt + 1) / 2, g.Hq, g.B);
     if (dbg) {
       if (g.Dp == 128) return launch_pp<128, 3, true>(mq, mk, mv, a, dim3(1), st);
       return launch_pp<64, 6, true>(mq, mk, mv, a, dim3(1), st);
     }
-    const dim3 grid2((nqt + 1) / 2, g.Hq, g.B);
     if (g.Dp == 128) return launch_pp<128, 3, false>(mq, mk, mv, a, grid2, st);
     return launch_pp<64, 6, false>(mq, mk, mv, a, grid2, st);
   }

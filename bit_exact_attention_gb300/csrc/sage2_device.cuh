@@ -434,6 +434,19 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return (uint32_t)r;
 }
 
+// Four e4m3 bytes of four floats in one word (round to nearest even, saturate to +-448):
+// byte i <- ai.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(w)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return w;
+}
+
 // 16-byte read-only global load that the compiler keeps in program order.
 __device__ __forceinline__ float4 ldg_nc_v4(const float *p) {
   float4 v;

@@ -1,9 +1,9 @@
 """CPU models of the attention kernels' synchronisation (bit_exact_attention_gb300/csrc/
-sage2_attention.cu). For attn_pp, the two-tile kernel, the model has a producer, an event-driven
-MMA issuer, an in-order tensor pipe with commit-to-mbarrier, and the softmax warps of both
-tiles. For attn_fwd, the one-tile kernel, it has two issuers with their own pipes, softmax and
-fold warps, a 4-slot alpha ring and double-buffered P~ and R. In both, the agents meet on
-mbarriers that are waited on by phase parity, as the hardware does.
+sage2_attention.cu). For attn_pp, the two-tile kernel, the model has a producer, a Q K^T issuer
+and a P~V issuer (separate threads, so separate in-order pipes whose commits track only their own
+MMAs), and the softmax warps of both tiles. For attn_fwd, the one-tile kernel, it has two issuers
+with their own pipes, softmax and fold warps, a 4-slot alpha ring and double-buffered P~ and R.
+In both, the agents meet on mbarriers that are waited on by phase parity, as the hardware does.
 
 Random interleavings (seeded) are checked for:
   * parity aliasing: a wait must only pass once the awaited phase has completed, and not when
@@ -12,10 +12,10 @@ Random interleavings (seeded) are checked for:
     rewritten once every reader of the old contents is done, and only read once written;
   * deadlock: every run finishes.
 The models follow the kernels' conditions one for one. Each has deliberately broken variants
-that must be caught. For the two-tile kernel these are: the last-tile wait for PV(T-2) removed,
-and QK issued without PV(n-2) issued. For the one-tile kernel: the R-free wait removed, and a
-single-slot alpha ring (a 2-slot ring fails as well, while 3 would do; the kernel keeps 4 for
-mask indexing).
+that must be caught. For the two-tile kernel these are: QK(n) issued without waiting for
+PV(n-2) to complete, and one P~V completion barrier per tile instead of one per P~ buffer. For
+the one-tile kernel: the R-free wait removed, and a single-slot alpha ring (a 2-slot ring fails
+as well, while 3 would do; the kernel keeps 4 for mask indexing).
 """
 from __future__ import annotations
 
@@ -49,26 +49,36 @@ class Bar:
 
 
 class Model:
-    def __init__(self, T0, T1, ST, W, rng, resc_p, last_tile_wait=True, qk_after_pv=True):
+    """attn_pp's protocol. QK_t(n) is issued once the softmax read S_t(n-1), K(n) landed and
+    PV_t(n-2) completed; PV_t(n) once P~_t(n) is written; each issuer gives a stage its own
+    arrival once all its products reading the stage are issued. pv_done[t][b] completes for the
+    PVs of P~ buffer b. The softmax rescales O_t after waiting for PV_t(j-1)."""
+
+    def __init__(self, T0, T1, ST, W, rng, resc_p, qk_after_pv=True, pv_bar_per_buffer=True):
         self.T, self.ST, self.W, self.rng = (T0, T1), ST, W, rng
         self.Tmax = max(T0, T1)
-        self.resc_p, self.last_tile_wait, self.qk_after_pv = resc_p, last_tile_wait, qk_after_pv
+        self.resc_p, self.qk_after_pv = resc_p, qk_after_pv
         B = Bar
         self.kv_full = [B(f"kv_full{s}", 1) for s in range(ST)]
-        self.kv_empty = [B(f"kv_empty{s}", 1) for s in range(ST)]
+        self.kv_empty = [B(f"kv_empty{s}", 2) for s in range(ST)]
         self.s_full = [B(f"s_full{t}", 1) for t in range(2)]
         self.s_free = [B(f"s_free{t}", W) for t in range(2)]
         self.p_full = [[B(f"p_full{t}{b}", W) for b in range(2)] for t in range(2)]
-        self.pv_done = [B(f"pv_done{t}", 1) for t in range(2)]
-        self.tok = [[B(f"tok{t}{w}", 1) for w in range(W)] for t in range(2)]
-        self.pipe = []                       # in-order tensor pipe: MMAs and commits
+        if pv_bar_per_buffer:
+            self.pv_done = [[B(f"pv_done{t}{b}", 1) for b in range(2)] for t in range(2)]
+            self.pv_phase = lambda n: n >> 1
+        else:  # one barrier per tile, completed by every PV
+            one = [B(f"pv_done{t}", 1) for t in range(2)]
+            self.pv_done = [[one[t], one[t]] for t in range(2)]
+            self.pv_phase = lambda n: n
+        self.pipes = {"qk": [], "pv": []}   # one in-order pipe per issuing thread
         self.stage = [None] * ST             # KV tile held by each stage
         self.stage_users = {}                # tile -> readers not yet done
         self.S = [None, None]                # QK index whose result S_t holds
         self.s_read = [[-1] * W for _ in range(2)]   # last S_t(j) read by each warp
         self.P = [[[None] * W for _ in range(2)] for _ in range(2)]  # P~ tile in buffer
         self.pv_completed = [0, 0]
-        self.events = 0                      # steps taken by agents other than the issuer
+        self.events = 0                      # steps taken by agents other than the issuers
 
     # ------------------------------------------------------------ helpers
     def use_stage(self, n, who):
@@ -78,6 +88,10 @@ class Model:
 
     def release_stage_user(self, n, who):
         self.stage_users[n].discard(who)
+
+    def pv_wait(self, t, n):
+        """The barrier and phase that PV_t(n)'s completion moves."""
+        return self.pv_done[t][n & 1], self.pv_phase(n)
 
     # ------------------------------------------------------------ agents (generators)
     def producer(self):
@@ -97,81 +111,89 @@ class Model:
             self.stage_users[j] = users
             yield ("act", self.kv_full[s].arrive)
 
-    def issuer(self):
-        nq, np_, ne = [0, 0], [0, 0], 0
-        while np_[0] < self.T[0] or np_[1] < self.T[1]:
-            progress = False
-            start = self.events
+    def release(self, ne, done, pipe):
+        while ne < self.Tmax and (ne >= self.T[0] or done[0] > ne) and \
+                (ne >= self.T[1] or done[1] > ne):
+            self.pipes[pipe].append(("commit", self.kv_empty[ne % self.ST]))
+            ne += 1
+        return ne
+
+    def qk_issuer(self):
+        nq, ne = [0, 0], 0
+        while nq[0] < self.T[0] or nq[1] < self.T[1]:
+            progress, start = False, self.events
             for t in range(2):
-                T = self.T[t]
+                n = nq[t]
+                if n >= self.T[t]:
+                    continue
+                ok = n == 0 or self.s_free[t].passes(n - 1)
+                if ok and self.qk_after_pv and n >= 2:
+                    yield ("poll", True)  # a separate test: other agents move in between
+                    ok = self.pv_wait(t, n - 2)[0].passes(self.pv_wait(t, n - 2)[1])
+                if ok:
+                    yield ("poll", True)
+                    ok = self.kv_full[n % self.ST].passes(n // self.ST)
+                if ok:
+                    if n > 0 and min(self.s_read[t]) < n - 1:
+                        raise Hazard(f"QK{t}({n}) issued before S{t}({n - 1}) was read")
+                    self.pipes["qk"] += [("QK", t, n), ("commit", self.s_full[t])]
+                    nq[t] += 1
+                    progress = True
+                    ne = self.release(ne, nq, "qk")
+            yield ("poll", progress or self.events != start)
+
+    def pv_issuer(self):
+        np_, ne = [0, 0], 0
+        while np_[0] < self.T[0] or np_[1] < self.T[1]:
+            progress, start = False, self.events
+            for t in range(2):
                 n = np_[t]
-                if n < nq[t] and self.p_full[t][n & 1].passes(n >> 1):
+                if n < self.T[t] and self.p_full[t][n & 1].passes(n >> 1):
+                    yield ("poll", True)
+                    if not self.kv_full[n % self.ST].passes(n // self.ST):
+                        continue
                     for w in range(self.W):
                         if self.P[t][n & 1][w] != n:
                             raise Hazard(f"PV{t}({n}) issued but warp {w}'s P~ buffer holds "
                                          f"{self.P[t][n & 1][w]}")
-                    self.pipe.append(("PV", t, n))
-                    self.pipe.append(("commit", self.pv_done[t]))
+                    bar, _ = self.pv_wait(t, n)
+                    self.pipes["pv"] += [("PV", t, n), ("commit", bar)]
                     np_[t] += 1
                     progress = True
-                    while ne < self.Tmax and (ne >= self.T[0] or np_[0] > ne) and \
-                            (ne >= self.T[1] or np_[1] > ne):
-                        self.pipe.append(("commit", self.kv_empty[ne % self.ST]))
-                        ne += 1
-                # the tests are separate instructions: other agents move in between
-                yield ("poll", True)
-                n = nq[t]
-                pv_ok = (np_[t] >= n - 1) if self.qk_after_pv else True
-                if n < T and pv_ok and (n == 0 or self.s_free[t].passes(n - 1)) and \
-                        self.kv_full[n % self.ST].passes(n // self.ST):
-                    if n > 0 and min(self.s_read[t]) < n - 1:
-                        raise Hazard(f"QK{t}({n}) issued before S{t}({n - 1}) was read")
-                    self.pipe.append(("QK", t, n))
-                    self.pipe.append(("commit", self.s_full[t]))
-                    nq[t] += 1
-                    progress = True
-            # idle only if nothing else moved during this pass either
+                    ne = self.release(ne, np_, "pv")
             yield ("poll", progress or self.events != start)
 
-    def pipe_step(self):
-        kind = self.pipe[0]
-        if kind[0] == "commit":
-            # completes once everything before it has completed: it is at the head
-            self.pipe.pop(0)
+    def pipe_step(self, name):
+        kind = self.pipes[name].pop(0)
+        if kind[0] == "commit":  # at the head: everything issued before it has completed
             kind[1].arrive()
             return
+        _, t, n = kind
         if kind[0] == "QK":
-            _, t, n = kind
             self.use_stage(n, f"QK{t}({n})")
             self.S[t] = n
             self.release_stage_user(n, ("QK", t))
         else:
-            _, t, n = kind
             self.use_stage(n, f"PV{t}({n})")
             if self.pv_completed[t] != n:
                 raise Hazard(f"PV{t}({n}) out of order")
             self.pv_completed[t] += 1
             self.release_stage_user(n, ("PV", t))
-        self.pipe.pop(0)
 
     def softmax(self, t, w):
-        T, other = self.T[t], self.T[1 - t]
+        T = self.T[t]
         for j in range(T):
             yield ("wait", self.s_full[t], j)
             if self.S[t] != j:
                 raise Hazard(f"softmax{t}.{w} reads S{t}({j}) but S holds {self.S[t]}")
             self.s_read[t][w] = j
             yield ("act", self.s_free[t].arrive)
-            yield ("wait", self.kv_full[j % self.ST], j // self.ST)
-            if (j >= 1 and j - 1 < other) if t == 0 else (j < other):
-                yield ("wait", self.tok[t][w], j - 1 if t == 0 else j)
-            self.use_stage(j, f"softmax{t}.{w} DeltaS({j})")
+            self.use_stage(j, f"softmax{t}.{w} DeltaS({j})")  # landed: QK_t(j) waited for it
             self.release_stage_user(j, ("SM", t, w))
-            yield ("act", self.tok[1 - t][w].arrive)
-            resc = j > 0 and self.rng.random() < self.resc_p
-            if resc or (self.last_tile_wait and j > 0 and j == T - 1):
-                yield ("wait", self.pv_done[t], j - 1)
-                if resc and self.pv_completed[t] != j:
+            if j > 0 and self.rng.random() < self.resc_p:
+                bar, ph = self.pv_wait(t, j - 1)
+                yield ("wait", bar, ph)
+                if self.pv_completed[t] != j:
                     raise Hazard(f"softmax{t}.{w} rescales O{t} at {j} with "
                                  f"{self.pv_completed[t]} PVs complete")
             if self.pv_completed[t] < j - 1:
@@ -179,18 +201,19 @@ class Model:
             self.P[t][j & 1][w] = j
             yield ("act", self.p_full[t][j & 1].arrive)
         if T > 0:
-            yield ("wait", self.pv_done[t], T - 1)
+            bar, ph = self.pv_wait(t, T - 1)
+            yield ("wait", bar, ph)
             if self.pv_completed[t] != T:
                 raise Hazard(f"epilogue{t}.{w} reads O{t} with {self.pv_completed[t]} of {T} PVs")
 
     # ------------------------------------------------------------ scheduler
-    def run(self, max_steps=200000):
-        agents = {"producer": self.producer(), "issuer": self.issuer()}
+    def run(self, max_steps=300000):
+        agents = {"producer": self.producer(), "qk": self.qk_issuer(), "pv": self.pv_issuer()}
         for t in range(2):
             for w in range(self.W):
                 agents[f"sm{t}{w}"] = self.softmax(t, w)
         pending = {k: None for k in agents}  # the action each agent is blocked on
-        idle_issuer = False
+        idle = set()                         # issuers that polled without progress
         for _ in range(max_steps):
             runnable = []
             for k, req in pending.items():
@@ -199,29 +222,24 @@ class Model:
                 if req is None:
                     runnable.append(k)
                 elif req[0] == "wait":
-                    bar, n = req[1], req[2]
-                    if (bar.c & 1) != (n & 1):
+                    if (req[1].c & 1) != (req[2] & 1):
                         runnable.append(k)
                 elif req[0] == "poll":
-                    if not (idle_issuer and not req[1]):
+                    if not (k in idle and not req[1]):
                         runnable.append(k)
-            if self.pipe:
-                runnable.append("pipe")
+            runnable += [("pipe", p) for p in ("qk", "pv") if self.pipes[p]]
             if not runnable:
                 if not agents:
                     return
-                if "issuer" in agents and pending["issuer"] and pending["issuer"][0] == "poll":
-                    # the issuer polled without progress and nothing else can move
-                    raise Hazard("deadlock: " + ", ".join(
-                        f"{k}:{pending[k][0]} {getattr(pending[k][1], 'name', '')}"
-                        for k in agents if pending[k]))
-                raise Hazard("deadlock")
+                raise Hazard("deadlock: " + ", ".join(
+                    f"{k}:{pending[k][0]} {getattr(pending[k][1], 'name', '')}"
+                    for k in agents if pending[k]))
             k = self.rng.choice(runnable)
-            idle_issuer = False
-            if k != "issuer":
+            if k not in ("qk", "pv"):
                 self.events += 1
-            if k == "pipe":
-                self.pipe_step()
+                idle.clear()
+            if isinstance(k, tuple):
+                self.pipe_step(k[1])
                 continue
             req = pending[k]
             if req is not None and req[0] == "wait":
@@ -235,11 +253,14 @@ class Model:
             if nxt[0] == "act":
                 nxt[1]()
                 pending[k] = None
-                idle_issuer = False
+                idle.clear()
             else:
                 pending[k] = nxt
-                if nxt[0] == "poll" and not nxt[1]:
-                    idle_issuer = True
+                if nxt[0] == "poll":
+                    if nxt[1]:
+                        idle.discard(k)
+                    else:
+                        idle.add(k)
         raise Hazard("step limit")
 
 
@@ -259,22 +280,22 @@ def _caught(**kw):
         rng = random.Random(seed)
         T0, T1 = rng.choice([(3, 4), (4, 4), (5, 6), (2, 3)])
         try:
-            Model(T0, T1, 3, W=2, rng=rng, resc_p=0.0, **kw).run()
+            Model(T0, T1, 3, W=2, rng=rng, resc_p=rng.choice([0.0, 0.5]), **kw).run()
         except Hazard:
             return True
     return False
 
 
-def test_model_catches_a_missing_last_tile_wait():
-    """Without the wait for PV(T-2) on the last tile, pv_done can lag two phases and the
-    epilogue's parity wait for PV(T-1) passes early: the model must find an interleaving."""
-    assert _caught(last_tile_wait=False)
-
-
-def test_model_catches_qk_issued_before_pv_two_back():
-    """QK(n) before PV(n-2) is issued lets the softmax refill the P~ buffer that PV(n-2) has not
-    read yet (and lets p_full run two phases ahead)."""
+def test_model_catches_qk_issued_before_pv_two_back_completed():
+    """QK(n) before PV(n-2) completes lets the softmax refill the P~ buffer that PV(n-2) has not
+    read yet."""
     assert _caught(qk_after_pv=False)
+
+
+def test_model_catches_one_pv_barrier_per_tile():
+    """With one P~V completion barrier per tile, a waiter for PV(n-2) can find PV(n-1) complete
+    as well: the barrier is two phases on, the parity test fails and the wait can never end."""
+    assert _caught(pv_bar_per_buffer=False)
 
 
 # ---------------------------------------------------------------------- one-tile kernel
