@@ -45,28 +45,38 @@ WORKLOADS.update({f"prefill_d{d}": W.scaled(W.PREFILL, W.PREFILL.nq, W.PREFILL.n
                   for d in (32, 64, 80, 96, 112)})
 FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor ratio (GB300)
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
-# DRAM bytes (read + write) of one attention launch, from a one-pass ncu capture of
-# dram__bytes_read.sum / dram__bytes_write.sum on the full workload (profiles/), valid only for
-# the kernel source they were taken on (sha256 prefix of csrc/sage2_attention.cu).
-MEASURED_TRAFFIC = {
-    ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage2"): (
-        "82ac2d604271a770", 746.45e6 + 246.30e6),
-    ("gqa_long_causal_B1_Hq32_Hkv8_N32768_D128_bf16", "sage1"): (
-        "82ac2d604271a770", 374.74e6 + 234.15e6),
-}
+# DRAM bytes (read + write) of one attention launch from a one-pass ncu capture, per workload and
+# path, with the sha256 prefix of csrc/sage2_attention.cu they were taken on (bench_traffic.json)
+TRAFFIC_FILE = os.path.join(ROOT, "bench_traffic.json")
+
+
+def load_traffic():
+    """{(workload, quant): (source sha256 prefix, bytes per launch)} from bench_traffic.json."""
+    out = {}
+    with open(TRAFFIC_FILE) as f:
+        for e in json.load(f)["entries"]:
+            out[(e["workload"], e["quant"])] = (e["source_sha16"],
+                                                e["dram_read_bytes"] + e["dram_write_bytes"])
+    return out
+
+
+MEASURED_TRAFFIC = load_traffic()
+
+
+def kernel_source_sha16():
+    import hashlib
+    src = os.path.join(ROOT, "bit_exact_attention_gb300", "csrc", "sage2_attention.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
 def measured_traffic(w, quant="sage2"):
     """The captured DRAM bytes per attention launch for this workload and path, or None when
     there is none or the kernel source has changed since the capture."""
-    import hashlib
     rec = MEASURED_TRAFFIC.get((w.name, quant))
     if rec is None:
         return None
-    src = os.path.join(ROOT, "bit_exact_attention_gb300", "csrc", "sage2_attention.cu")
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec[1] if digest == rec[0] else None
+    return rec[1] if kernel_source_sha16() == rec[0] else None
 
 
 def parse():
@@ -78,6 +88,10 @@ def parse():
     p.add_argument("--workload", default="gqa_long", choices=sorted(WORKLOADS))
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the per-workload measurements after the headline timing")
+    p.add_argument("--no-fp8-peak", action="store_true",
+                   help="skip the dense e4m3 GEMM peak measurement (torch._scaled_mm)")
     p.add_argument("--e2e-chunks", type=int, default=8,
                    help="kv-head chunks of the host-memory forward (copies overlap compute)")
     p.add_argument("--quant", default="sage2", choices=["sage2", "sage1"],
@@ -201,6 +215,13 @@ class ClockSampler:
                 "samples": len(rows), "window": window}
 
 
+def measured_hbm_gbs():
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+    except (OSError, KeyError, ValueError):
+        return 6800.0  # the recipe's fallback
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -245,6 +266,138 @@ def run_oracle_sample(w: W.Workload, x: dict, units, quant="sage2"):
 
 def sample_size(w: W.Workload) -> int:
     return 12 if max(w.nkv) >= 16384 else 32
+
+
+# ------------------------------------------------------------------ per-workload figures
+def visited_keys(nq, nkv, causal):
+    """Keys per (q head, Q block) whose DeltaS the prepass writes: every key of the KV tiles the
+    block visits (bottom-right causal alignment), summed over the blocks of one sequence."""
+    total = 0
+    nt = (nkv + 127) // 128
+    for qb in range((nq + 127) // 128):
+        if causal:
+            i_last = min(qb * 128 + 127, nq - 1)
+            j_max = i_last + (nkv - nq)
+            t = 0 if j_max < 0 else min(nt, j_max // 128 + 1)
+        else:
+            t = nt
+        total += min(nkv, t * 128)
+    return total
+
+
+def prepass_algorithmic_bytes(w: W.Workload) -> int:
+    """Bytes the prepass has to move at the least: Q, K and V read once (2 bytes an element),
+    their 8-bit codes written once (padded head dim), and DeltaS*c (4 bytes) written for every
+    (q head, Q block, visited key). Scales and means (under 1 % here) are left out."""
+    dp = 64 if w.d <= 64 else 128
+    tq, tkv = sum(w.nq), sum(w.nkv)
+    reads = 2 * w.d * (tq * w.hq + 2 * tkv * w.hkv)
+    writes = dp * (tq * w.hq + 2 * tkv * w.hkv)
+    writes += 4 * w.hq * sum(visited_keys(a, b, w.causal) for a, b in zip(w.nq, w.nkv))
+    return reads + writes
+
+
+def time_workload(S, w, dev, steps, warmup, flush, stream, qf):
+    """Prepass and attention of one workload through the C ABI, inputs resident on the device,
+    L2 flushed between steps: per-step CUDA-event times (ms) of both halves."""
+    x = W.make_inputs(w)
+    max_nq, max_nkv, tq, tkv = max(w.nq), max(w.nkv), sum(w.nq), sum(w.nkv)
+    q, k, v = (x[n].to(dev) for n in "qkv")
+    cu_q = torch.tensor(x["cu_q"], dtype=torch.int32, device=dev)
+    cu_kv = torch.tensor(x["cu_kv"], dtype=torch.int32, device=dev)
+    out = torch.empty(tq, w.hq, w.d, dtype=q.dtype, device=dev)
+    ws = S.alloc_workspace(S.workspace_size(w.batch, w.hq, w.hkv, max_nq, max_nkv, w.d, tq, tkv,
+                                            quant_flags=qf), dev)
+
+    def step():
+        S.prepass_varlen(q, k, v, cu_q, cu_kv, max_nq, max_nkv, ws, causal=w.causal,
+                         stream=stream, quant_flags=qf)
+        e[1].record(stream)
+        S.attention_varlen(out, ws, cu_q, cu_kv, w.hkv, max_nq, max_nkv, tkv, causal=w.causal,
+                           stream=stream, quant_flags=qf)
+
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for _ in range(warmup):
+        step()
+    pre, att = [], []
+    for _ in range(steps):
+        flush.zero_()
+        e[0].record(stream)
+        step()
+        e[2].record(stream)
+        torch.cuda.synchronize(dev)
+        pre.append(e[0].elapsed_time(e[1]))
+        att.append(e[1].elapsed_time(e[2]))
+    rc, raw = S.device_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"{w.name}: device status {rc} {raw:#x}")
+    return pre, att
+
+
+def per_config_figures(S, names, dev, flush, stream, qf, peak, hbm_gbs, steps=5, warmup=2):
+    """Kernel-only and whole-step TOPS, the attention kernel's fraction of `peak`, and the
+    prepass time and algorithmic GB/s, for each named workload (median of `steps`)."""
+    res = {}
+    for name in names:
+        w = WORKLOADS[name]
+        pre, att = time_workload(S, w, dev, steps, warmup, flush, stream, qf)
+        p_ms, a_ms = statistics.median(pre), statistics.median(att)
+        ops = w.metric_ops()
+        kern = ops / (a_ms / 1e3) / 1e12
+        gbs = prepass_algorithmic_bytes(w) / (p_ms / 1e3) / 1e9
+        res[w.name] = {"attention_ms": round(a_ms, 4), "prepass_ms": round(p_ms, 4),
+                       "kernel_only_tops": round(kern, 2),
+                       "step_tops": round(ops / ((p_ms + a_ms) / 1e3) / 1e12, 2),
+                       "roofline_frac": round(kern / peak, 4),
+                       "prepass_gbs": round(gbs, 1),
+                       "prepass_frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None,
+                       "metric_ops": ops, "steps": steps}
+    return res
+
+
+def fp8_dense_peak(dev, local, sustained_s=4.0):
+    """Dense e4m3 GEMM throughput on this GPU: torch._scaled_mm, 8192 x 8192 x 8192 with unit
+    scales and bf16 output, best of 10 (burst) and back to back for about `sustained_s`
+    seconds (sustained, SM clocks sampled meanwhile)."""
+    n = 8192
+    try:
+        g = torch.Generator(device=dev).manual_seed(0)
+        a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev, dtype=torch.float32)
+
+        def mm():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            mm()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(10):
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        flops = 2.0 * n ** 3
+        iters = max(10, int(sustained_s / (best / 1e3)))
+        clocks = ClockSampler(local)
+        clocks.start()
+        t0 = time.time()
+        e0.record()
+        for _ in range(iters):
+            mm()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        clk = clocks.stop(t0, t1)
+        return {"burst_tflops": round(flops / (best / 1e3) / 1e12, 1),
+                "sustained_tflops": round(flops * iters / (e0.elapsed_time(e1) / 1e3) / 1e12, 1),
+                "how": f"torch._scaled_mm e4m3 x e4m3 -> bf16, {n}^3: best of 10; {iters} back to "
+                       f"back", "clocks_sustained": clk}
+    except Exception as exc:  # a missing FP8 GEMM in this torch build: report, do not fail
+        return {"error": repr(exc)[:200]}
 
 
 # ------------------------------------------------------------------ our implementation
@@ -390,6 +543,21 @@ def run_ours(args, rank, world, local):
                                 "time-weighted)" if sage1 else
                                 f"{peak_src} bf16 burst x {FP8_OVER_BF16} (e4m3)"),
                 "frac_of_sustained": round(achieved / (bf16_sust * mix), 4)}
+    # the measured dense e4m3 GEMM rate beside the bf16 x 2 figure (both MMAs of the method run
+    # on e4m3; the v1 path's Q K^T does not, so it gets no such line)
+    if not sage1 and not args.no_fp8_peak and rank == 0:
+        fp8 = fp8_dense_peak(dev, local)
+        if "burst_tflops" in fp8:
+            fp8["frac_of_burst"] = round(achieved / fp8["burst_tflops"], 4)
+            fp8["frac_of_sustained"] = round(achieved / fp8["sustained_tflops"], 4)
+        roofline["fp8_measured"] = fp8
+
+    # every workload of the method, measured after the headline timing in the same process
+    per_config = None
+    if not args.no_per_config and rank == 0:
+        names = [x.name for x in W.ALL]
+        per_config = per_config_figures(S, names, dev, flush, stream, qf, peak,
+                                        measured_hbm_gbs())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -415,7 +583,7 @@ def run_ours(args, rank, world, local):
             "kernel_only_tops": round(ops / (att_mean / 1e3) / 1e12, 3),
             "prepass_ms": round(pre_mean, 4), "attention_ms": round(att_mean, 4),
             "wall_s": round(t_wall, 4),
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "per_config": per_config,
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": clk,
         }

@@ -14,8 +14,13 @@
  *      one per 32 consecutive K tokens (the thread-owned groups of the tensor-memory
  *      accumulator layout). Q K^T of the codes is exact (integer valued).
  *   3. V is quantized per channel to FP8 e4m3 (scale amax/448); P~ = e4m3(448 P).
- *   4. P~ V is accumulated per 128-key block into a fresh FP32 partial in tensor memory,
- *      then folded into an FP32 accumulator on the CUDA cores (two-level accumulation).
+ *   4. Two-level accumulation of P~ V: each 128-key block's FP8 products are summed by the
+ *      tensor core into an FP32 accumulator in tensor memory, and the running output stays
+ *      FP32 across blocks. The default kernel (two Q tiles per CTA) rescales the FP32 output
+ *      accumulator by alpha on the CUDA cores when a row maximum moves and lets the block's
+ *      MMA add into it; with SAGE2_ATTN_PP=0 in the environment (and for SAGE2_QUANT_SAGE1),
+ *      the one-tile kernel sums each block into a fresh FP32 partial and folds it into an FP32
+ *      output held in registers (O = alpha O + R).
  * Interface envelope (visual companion, Per-Thread INT4 Geometry, implementation panel):
  * GQA, different q and kv lengths, packed variable-length batches, head dim padded to
  * 64 or 128, head dims above 128 rejected.
@@ -25,7 +30,10 @@
  *     out [B, Nq, Hq, D]; varlen calls take the packed forms [total, H, D] with
  *     cu_seqlens (int32, B + 1 prefix sums). All row-major and contiguous.
  *   - q, k, v, out, workspace are DEVICE pointers owned by the caller; nothing is retained
- *     after a call returns. Pointers must be 16-byte aligned; the workspace 1024-byte aligned.
+ *     after a call returns (except by sage2_attn_fwd_noalloc, whose scratch array lives in the
+ *     library and keeps the last call's contents). Pointers, the workspace included, must be
+ *     16-byte aligned; the library aligns the workspace base up to 1024 bytes inside the call
+ *     (sage2_workspace_size() includes that slack).
  *   - in_dtype: SAGE2_FP16 or SAGE2_BF16. out_dtype: the input dtype or SAGE2_FP32.
  *   - D (the head dim of the tensors, called D0 in the comments) must satisfy 8 <= D <= 128
  *     and D % 8 == 0; it is computed as 64 (D <= 64) or 128 (D <= 128) with zero channels.

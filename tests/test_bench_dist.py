@@ -56,18 +56,38 @@ def test_single_rank_is_identity():
     assert bench.aggregate_value(2e12, 2.0, 1) == pytest.approx(1.0)
 
 
-def test_traffic_figures_match_their_profiles():
-    """The DRAM bytes that bench.py reports come from the captures summarised under profiles/:
-    the same kernel-source hash and the same counter values, one profile per path."""
-    import re
+def test_traffic_data_file_and_hash_guard(monkeypatch):
+    """bench.py takes its DRAM traffic figures from bench_traffic.json and reports one only while
+    the attention kernel's source has the hash that the figure was captured on."""
+    import json
 
     import bench
+    from bit_exact_attention_gb300 import workloads as W
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    files = {"sage2": "traffic_attn_pp_gqa_long_causal_B1_Hq32_Hkv8_N32768_D128.md",
-             "sage1": "traffic_attn_fwd_gqa_long_causal_B1_Hq32_Hkv8_N32768_D128.md"}
-    for (workload, quant), (digest, nbytes) in bench.MEASURED_TRAFFIC.items():
-        text = open(os.path.join(root, "profiles", files[quant])).read()
-        assert f"sha256 prefix `{digest}`" in text, (quant, digest)
-        rows = dict(re.findall(r"\| (dram__bytes_(?:read|write)\.sum) \| ([0-9.]+) MB \|", text))
-        got = (float(rows["dram__bytes_read.sum"]) + float(rows["dram__bytes_write.sum"])) * 1e6
-        assert abs(got - nbytes) <= 0.01e6, (quant, got, nbytes)
+    data = json.load(open(bench.TRAFFIC_FILE))
+    assert data["entries"]
+    for e in data["entries"]:
+        assert e["dram_read_bytes"] > 0 and e["dram_write_bytes"] > 0
+        assert len(e["source_sha16"]) == 16 and int(e["source_sha16"], 16) >= 0
+        assert os.path.exists(os.path.join(root, e["profile"])), e["profile"]
+    digest, nbytes = bench.MEASURED_TRAFFIC[(W.GQA_LONG.name, "sage2")]
+    monkeypatch.setattr(bench, "kernel_source_sha16", lambda: digest)
+    assert bench.measured_traffic(W.GQA_LONG) == nbytes
+    monkeypatch.setattr(bench, "kernel_source_sha16", lambda: "0" * 16)
+    assert bench.measured_traffic(W.GQA_LONG) is None
+
+
+def test_visited_keys_by_enumeration():
+    """The DeltaS entries counted for the prepass's algorithmic bytes: every key of every KV tile
+    a Q block visits, checked against a per-row enumeration of the bottom-right causal rule."""
+    import bench
+    for nq, nkv in [(1, 1), (300, 100), (100, 300), (256, 256), (1000, 777), (5, 4000)]:
+        for causal in (False, True):
+            want = 0
+            for qb in range((nq + 127) // 128):
+                last = -1
+                for i in range(qb * 128, min(nq, qb * 128 + 128)):
+                    jmax = nkv - 1 if not causal else min(nkv - 1, i + nkv - nq)
+                    last = max(last, jmax)
+                want += 0 if last < 0 else min(nkv, (last // 128 + 1) * 128)
+            assert bench.visited_keys(nq, nkv, causal) == want, (nq, nkv, causal)
