@@ -8,8 +8,11 @@ the prepass (sage2_quant_flags); the attention kernel is unchanged. For every se
     within the hardware exponential's error of an e4m3 rounding midpoint; each such code is
     one e4m3 step off;
   * the output is within relative L1 1e-3 of the oracle's emulation with the same switches,
-    and every element within 2e-3 or within the one-step bound max|V| / 8 (a P~ code one
-    e4m3 step off moves a row by at most 1/8 of that key's weight; the weights sum to 1);
+    and every element within 2e-3, except rows proven to differ only through such flips: the
+    row recomputed from the GPU's own P~ codes matches the GPU within 2e-3, and each differing
+    code is a located midpoint flip (parity_util.check_forward_proven). On the un-smoothed
+    settings rows are sharply peaked, so one flip of a dominant key can move a row by more
+    than 2e-3;
   * against exact attention the GPU errs as the emulation does, and the ordering the pages
     claim holds on the GPU too (each repair lowers the error).
 
@@ -31,7 +34,7 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import (GpuCase, bits, c32_of, check_forward_with_flips, compare_p_codes, kv_tiles,
+from parity_util import (GpuCase, bits, c32_of, check_forward_proven, compare_p_codes, kv_tiles,
                          metrics, pad_starts)
 
 pytestmark = pytest.mark.gpu
@@ -185,7 +188,7 @@ def test_forward_matches_emulation_with_switches(name, setting):
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle.attention_emulated(*_args(w, x), **kw)
-    check_forward_with_flips(out, emu, x)
+    check_forward_proven(g, w, x, out, emu, kw)
 
 
 def test_dense_entry_with_switches_equals_varlen():
