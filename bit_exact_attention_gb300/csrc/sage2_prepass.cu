@@ -13,8 +13,9 @@
 //      [kv head][channel][token] so both operands of the P~V MMA are K-major.
 //   4. q_quant: per block of 128 rows the mean qmean; Q~ = fl32(Q - qmean); one scale per
 //      row; codes as for K.
-//   5. delta_s: DeltaS = qmean . K~ in FP32, one fused multiply-add per channel in channel
-//      order (register-blocked tiles), stored pre-multiplied by c = log2(e) * sm_scale.
+//   5. delta_s_tc: DeltaS = qmean . K~ on the tensor cores (both operands split exactly into
+//      three bf16 pieces, the six leading piece products summed in FP32), stored multiplied by
+//      c = log2(e) * sm_scale.
 // Every padded position (channels D0..Dp, tokens past a sequence end up to its 128-row
 // boundary) is written with zero codes and zero scales.
 // Ablation switches (sage2_quant_flags) change only what these kernels write: a zero K
@@ -24,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "sage2_device.cuh"
@@ -517,174 +519,310 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
 }
 
 // ------------------------------------------------------------------ 5. DeltaS
-// A small FP32 GEMM per (sequence, kv head): rows are the (Q block, q head of the group)
-// pairs, ordered Q-block-major (r = qb * g + head), columns the keys, inner dimension the
-// channels. A CTA computes a ROWS x KEYS tile (ROWS * KEYS = 128 * 128; the launcher picks the
-// row-tile height that wastes the fewest rows, so a kv head with few (Q block, head) rows does
-// not compute a 128-row tile of padding). grid (key tiles, row tiles, B * Hkv), block 256.
-// Thread (tr, tk) owns 8 rows and the 8 keys {4tk + e, KEYS/2 + 4tk + e : e < 4} (so a warp's
-// shared-memory reads are contiguous 16-byte pieces). Channels are staged CH at a time in
-// shared memory (two buffers, one barrier per chunk), transposed, converted to FP32 and
-// smoothed; a chunk's global loads are issued two chunks ahead of its FMAs. Every output is one
-// FMA chain in increasing channel order (the same operation sequence as the definition, so the
-// result is bit-identical to it). Causal: a CTA whose rows visit none of its keys returns; a
-// warp whose rows visit none of them skips the FMAs; an output whose 128-key tile its Q block
-// does not visit is not written.
-template <int ROWS>
-struct DsTile {
-  static constexpr int kKeys = kBQ * kBKV / ROWS;  // 128, 256 or 512
-  static constexpr int kCh = ROWS == 32 ? 8 : 16;  // channels per staged chunk
-  static constexpr int kTk = kKeys / 8;            // threads along the keys
-  static constexpr int kKVec = kKeys * (kCh / 8) / 256;              // 8-channel K vectors
-  static constexpr int kQVec = (ROWS * (kCh / 4) + 255) / 256;       // 4-channel Q-mean vectors
-  static_assert(kTk * (ROWS / 8) == 256, "256 threads, 8 x 8 outputs each");
-  static_assert(kKVec * 256 == kKeys * (kCh / 8), "whole K vectors per thread");
+// DeltaS on the tensor cores. Per (sequence, kv head) a GEMM: rows are the (Q block, q head of
+// the group) pairs, ordered Q-block-major (r = qb * grp + head), columns the keys, inner
+// dimension the channels; out[r][j] = fl32(c * fl32(qmean_r . K~_j)), K~ = fl32(K - kmean).
+// Each FP32 operand is split exactly into three bf16 pieces (x = x1 + x2 + x3 with truncation:
+// x1 the top 8 significant bits, x2 the next 8, x3 the last 8, each exactly a bf16), and the
+// six products xa_i * xb_j with i + j <= 4 (1-based) are summed by kind::f16 MMAs into one FP32
+// accumulator in tensor memory, smallest first. Each piece product is exact; the three dropped
+// ones are below 2^-23 of |qmean_d K~_jd|, and the accumulator rounds once per MMA step
+// (6 x D / 16 steps), so the result lies within about 50 units of 2^-24 of
+// sum_d |qmean_d K~_jd| of the exact dot product.
+// One CTA per (128-row tile, chunk of kDsChunk key tiles, sequence x kv head); warps:
+//   0-7  per key tile K~ of 32 keys x half the channels per warp: each load instruction reads
+//        whole 128-byte row segments (DP / 16 lanes per segment), and each lane splits its
+//        8 channels and stores the three 16-byte pieces straight into their swizzled places in
+//        one of two shared buffers (the split is elementwise, so no lane needs another's
+//        data); warps 0-3 first put the qmean pieces into tensor memory (thread = row = TMEM
+//        lane, 16 channels at a time);
+//   8-11 epilogue: one accumulator row per thread, 32 columns at a time times c, through a
+//        small swizzled shared block so that the global stores are whole 128-byte segments,
+//        for the key tiles each row's Q block visits;
+//   12   MMA issuer (one lane); it also allocates tensor memory.
+// Tensor memory: the qmean pieces at [0, 3 DP / 2), two 128-column accumulators at 256 and 384.
+constexpr int kDsChunk = 8;  // key tiles per CTA
+constexpr int kDsThreads = 416, kDsLoadWarps = 8, kDsMmaWarp = 12;  // epilogue: warps 8-11
+
+template <int DP>
+struct DsPlan {
+  static constexpr int kPiece = 128 * DP * 2;         // one bf16 piece of 128 keys x DP
+  static constexpr int kBuf = 3 * kPiece;             // the three pieces
+  static constexpr int kB = 0;                        // [2][3][DP / 64][128][128 B] (swizzled)
+  static constexpr int kStage = kB + 2 * kBuf;        // float [4 warps][32][32] (swizzled)
+  static constexpr int kMu = kStage + 4 * 32 * 32 * 4;  // float [DP]
+  static constexpr int kBar = kMu + DP * 4;           // a_full, b_full[2], b_empty[2],
+  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 1;  // acc_full[2], acc_empty[2], drain
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16 + 1024;
+  static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
 
-template <int DP, int ROWS, bool BF16>
-__global__ void __launch_bounds__(256, 2) delta_s(PrepassArgs a) {
-  using T = DsTile<ROWS>;
-  constexpr int KEYS = T::kKeys, CH = T::kCh, NCH = DP / CH;
-  __shared__ __align__(16) float Qs[2][CH][ROWS];
-  __shared__ __align__(16) float Ks[2][CH][KEYS];
-  __shared__ float mu_s[DP];
+// Instruction descriptor, kind::f16 with A = B = bf16, D = f32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// x = p0 + p1 + p2 exactly, each a bf16 (as its 16 bits): truncation to the top 8 significant
+// bits, twice, leaves at most 8 significant bits in the last remainder.
+__device__ __forceinline__ void split3(float x, uint32_t &p0, uint32_t &p1, uint32_t &p2) {
+  const uint32_t b0 = __float_as_uint(x) & 0xFFFF0000u;
+  const float r1 = __fsub_rn(x, __uint_as_float(b0));
+  const uint32_t b1 = __float_as_uint(r1) & 0xFFFF0000u;
+  const float r2 = __fsub_rn(r1, __uint_as_float(b1));
+  p0 = b0 >> 16;
+  p1 = b1 >> 16;
+  p2 = __float_as_uint(r2) >> 16;
+}
+
+__device__ __forceinline__ bool ds_wait(uint64_t *bar, uint32_t parity, const AbortCtx &ab,
+                                        int site) {
+  return __shfl_sync(0xffffffffu, mbar_wait(bar, parity, ab, site) ? 1 : 0, 0) != 0;
+}
+
+template <int DP, bool BF16>
+__global__ void __launch_bounds__(kDsThreads, 1) delta_s_tc(PrepassArgs a) {
+  using P = DsPlan<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Geometry &g = a.g;
-  const int k0 = blockIdx.x * KEYS, rt = blockIdx.y;
+  const int rt = blockIdx.y;
   const int b = blockIdx.z / g.Hkv, hk = blockIdx.z % g.Hkv;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
-  if (!s.ok || k0 >= s.nkv || s.nq == 0) return;
+  if (!s.ok || s.nkv == 0 || s.nq == 0) return;
   const int grp = g.Hq / g.Hkv;
-  const int nqb = (s.nq + kBQ - 1) / kBQ;
-  const int nrows = grp * nqb;
-  const int r0 = rt * ROWS;
+  const int nrows = grp * ((s.nq + kBQ - 1) / kBQ);
+  const int r0 = rt * 128;
   if (r0 >= nrows) return;
-  const int qb_last = min(nrows - 1, r0 + ROWS - 1) / grp;
-  if (g.causal && kv_tiles_for(qb_last, s.nq, s.nkv, 1) <= k0 / kBKV) return;
+  const int ntile_kv = (s.nkv + kBKV - 1) / kBKV;
+  const int qb_last = min(nrows - 1, r0 + 127) / grp;
+  const int t_end_all = g.causal ? kv_tiles_for(qb_last, s.nq, s.nkv, 1) : ntile_kv;
+  const int t0 = blockIdx.x * kDsChunk, t1 = min(t_end_all, t0 + kDsChunk);
+  if (t0 >= t1) return;
+  const int nt = t1 - t0;
 
-  const int tid = threadIdx.x;
-  const int tr = tid / T::kTk, tk = tid % T::kTk;
-  for (int d = tid; d < DP; d += 256) mu_s[d] = a.w.kmean[((size_t)b * g.Hkv + hk) * DP + d];
-
-  // loader roles. K: vector v = tid + 256 i covers key k0 + v % KEYS, channels
-  // 8 * (v / KEYS) .. + 7 of the chunk. Q means: vector v = tid + 256 i < ROWS * CH / 4 covers
-  // row r0 + v % ROWS, channels 4 * (v / ROWS) .. + 3.
-  const size_t krow_stride = (size_t)g.Hkv * g.D0;
-  uint4 kreg[T::kKVec];
-  float4 qreg[T::kQVec];
-  auto load_chunk = [&](int c0) {
-#pragma unroll
-    for (int i = 0; i < T::kKVec; ++i) {
-      const int v = tid + 256 * i;
-      const int key = k0 + v % KEYS, ch = c0 + 8 * (v / KEYS);
-      kreg[i] = (key < s.nkv && ch < g.D0)
-                    ? __ldg(reinterpret_cast<const uint4 *>(
-                          a.k + (size_t)(s.kv0 + key) * krow_stride + (size_t)hk * g.D0 + ch))
-                    : make_uint4(0u, 0u, 0u, 0u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float *mu_s = reinterpret_cast<float *>(smem + P::kMu);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::kBar);
+  uint64_t *a_full = bars, *b_full = bars + 1, *b_empty = bars + 3, *acc_full = bars + 5,
+           *acc_empty = bars + 7, *drain = bars + 9;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kMisc + 4);
+  for (int d = tid; d < DP; d += kDsThreads)
+    mu_s[d] = a.w.kmean[((size_t)b * g.Hkv + hk) * DP + d];
+  if (tid == 0) {
+    mbar_init(a_full, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b_full[i], kDsLoadWarps);
+      mbar_init(&b_empty[i], 1);
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
     }
-#pragma unroll
-    for (int i = 0; i < T::kQVec; ++i) {
-      const int v = tid + 256 * i;
-      const int r = r0 + v % ROWS, ch = c0 + 4 * (v / ROWS);
-      qreg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (v < ROWS * (CH / 4) && r < nrows) {
-        const int qb = r / grp, hq = hk * grp + r % grp;
-        qreg[i] = __ldg(reinterpret_cast<const float4 *>(
-            a.w.qmean + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * DP + ch));
-      }
-    }
-  };
-  auto store_chunk = [&](int c0, int buf) {
-#pragma unroll
-    for (int i = 0; i < T::kKVec; ++i) {
-      const int v = tid + 256 * i;
-      const int kl = v % KEYS, cl = 8 * (v / KEYS);
-      float x[8];
-      unpack8<BF16>(kreg[i], x);
-      const bool ok = k0 + kl < s.nkv && c0 + cl < g.D0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        Ks[buf][cl + e][kl] = ok ? __fsub_rn(x[e], mu_s[c0 + cl + e]) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < T::kQVec; ++i) {
-      const int v = tid + 256 * i;
-      if (v < ROWS * (CH / 4)) {
-        const int rl = v % ROWS, cl = 4 * (v / ROWS);
-        Qs[buf][cl][rl] = qreg[i].x;
-        Qs[buf][cl + 1][rl] = qreg[i].y;
-        Qs[buf][cl + 2][rl] = qreg[i].z;
-        Qs[buf][cl + 3][rl] = qreg[i].w;
-      }
-    }
-  };
-
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  // A warp whose rows all lie past the end, or (causal) none of whose rows visits this CTA's
-  // first key tile, skips the FMAs: none of its outputs is written. Warp-uniform.
-  bool warp_busy;
-  {
-    const int w_tr_max = (32 * (tid / 32) + 31) / T::kTk;
-    const int w_row_min = r0 + (32 * (tid / 32)) / T::kTk * 8, w_row_max = r0 + w_tr_max * 8 + 7;
-    warp_busy = w_row_min < nrows;
-    if (warp_busy && g.causal)
-      warp_busy = kv_tiles_for(min(w_row_max, nrows - 1) / grp, s.nq, s.nkv, 1) > k0 / kBKV;
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
   }
-
-  load_chunk(0);
-  __syncthreads();  // mu_s
-  store_chunk(0, 0);
-  if (NCH > 1) load_chunk(CH);
+  if (warp == kDsMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-#pragma unroll 1
-  for (int ci = 0; ci < NCH; ++ci) {
-    const int buf = ci & 1;
-    if (ci + 1 < NCH) {  // the other buffer was last read before the previous barrier
-      store_chunk((ci + 1) * CH, buf ^ 1);
-      if (ci + 2 < NCH) load_chunk((ci + 2) * CH);  // in flight during the FMAs below
-    }
-    if (warp_busy) {
-#pragma unroll
-      for (int d = 0; d < CH; ++d) {
-        const float4 qa = *reinterpret_cast<const float4 *>(&Qs[buf][d][tr * 8]);
-        const float4 qc = *reinterpret_cast<const float4 *>(&Qs[buf][d][tr * 8 + 4]);
-        const float4 ka = *reinterpret_cast<const float4 *>(&Ks[buf][d][tk * 4]);
-        const float4 kc = *reinterpret_cast<const float4 *>(&Ks[buf][d][KEYS / 2 + tk * 4]);
-        const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
-        const float kk[8] = {ka.x, ka.y, ka.z, ka.w, kc.x, kc.y, kc.z, kc.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; j += 2)  // packed: two independent, correctly rounded FMAs
-            fma2(acc[i][j], acc[i][j + 1], qq[i], qq[i], kk[j], kk[j + 1], acc[i][j], acc[i][j + 1]);
-      }
-    }
-    __syncthreads();  // chunk ci + 1 is staged; chunk ci's buffer is free
-  }
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const AbortCtx ab{abort_flag, a.w.status};
+  constexpr uint32_t kColA = 0, kColAcc = 256;
 
-  const int ntile_kv = (s.nkv + kBKV - 1) / kBKV;  // written tiles stay inside the row stride
+  if (warp < kDsLoadWarps) {
+    // ------------------------------------------------------------ qmean pieces, then K~ tiles
+    if (warp < 4) {
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      const int r = r0 + warp * 32 + lane;
+      const bool row_ok = r < nrows;
+      const float4 *src = reinterpret_cast<const float4 *>(
+          a.w.qmean + ((size_t)(hk * grp + (row_ok ? r % grp : 0)) * a.L.nqblk + s.qpad0 / kBQ +
+                       (row_ok ? r / grp : 0)) * DP);
+#pragma unroll 1
+      for (int c = 0; c < DP / 16; ++c) {  // 16 channels = 8 columns per piece
+        float qv[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = r0 + tr * 8 + i;
-    if (rr >= nrows) break;
-    const int qb = rr / grp, hq = hk * grp + rr % grp;
-    const int vis = g.causal ? kv_tiles_for(qb, s.nq, s.nkv, 1) : ntile_kv;
-    float *row = a.w.dsc + ((size_t)hq * a.L.nqblk + s.qpad0 / kBQ + qb) * a.L.nkv_pad;
+        for (int e = 0; e < 4; ++e) {
+          const float4 f = row_ok ? __ldg(src + 4 * c + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+          qv[4 * e] = f.x;
+          qv[4 * e + 1] = f.y;
+          qv[4 * e + 2] = f.z;
+          qv[4 * e + 3] = f.w;
+        }
+        uint32_t w0[8], w1[8], w2[8];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int key = k0 + half * (KEYS / 2) + tk * 4;  // 4 keys, one 128-key tile
-      if (key / kBKV >= vis) continue;
-      float4 o;
-      o.x = __fmul_rn(acc[i][4 * half + 0], g.c32);
-      o.y = __fmul_rn(acc[i][4 * half + 1], g.c32);
-      o.z = __fmul_rn(acc[i][4 * half + 2], g.c32);
-      o.w = __fmul_rn(acc[i][4 * half + 3], g.c32);
-      *reinterpret_cast<float4 *>(row + key) = o;
+        for (int e = 0; e < 8; ++e) {
+          uint32_t a0, a1, a2, b0, b1, b2;
+          split3(qv[2 * e], a0, a1, a2);
+          split3(qv[2 * e + 1], b0, b1, b2);
+          w0[e] = a0 | (b0 << 16);
+          w1[e] = a1 | (b1 << 16);
+          w2[e] = a2 | (b2 << 16);
+        }
+        tmem_st8(tbase + lane_base + kColA + 8 * c, w0);
+        tmem_st8(tbase + lane_base + kColA + DP / 2 + 8 * c, w1);
+        tmem_st8(tbase + lane_base + kColA + DP + 8 * c, w2);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_full);
     }
+    // warp w: keys 32 (w % 4) .. + 31, channel half w / 4. Lane l: chunk c8 = half * CPR +
+    // l % CPR of the keys 32 (w % 4) + RPI i + l / CPR, i < CPR (CPR 8-channel chunks per half
+    // row, RPI rows per instruction)
+    constexpr int CPR = DP / 16, RPI = 32 / CPR;
+    const int c8 = (warp >> 2) * CPR + lane % CPR;
+    const int key0 = (warp & 3) * 32 + lane / CPR;
+    const bool ch_live = c8 * 8 < g.D0;
+    float mu8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mu8[e] = mu_s[c8 * 8 + e];
+    const int off_blk = (c8 >> 3) * 16384;
+    const size_t krow_stride = (size_t)g.Hkv * g.D0;
+    bool ok = true;
+#pragma unroll 1
+    for (int t = 0; t < nt && ok; ++t) {
+      const int buf = t & 1;
+      const int kbase = (t0 + t) * kBKV;
+      uint4 raw[CPR];
+#pragma unroll
+      for (int i = 0; i < CPR; ++i) {
+        const int key = kbase + key0 + RPI * i;
+        raw[i] = (key < s.nkv && ch_live)
+                     ? __ldg(reinterpret_cast<const uint4 *>(
+                           a.k + (size_t)(s.kv0 + key) * krow_stride + (size_t)hk * g.D0 + c8 * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (t >= 2 && !(ok = ds_wait(&b_empty[buf], ((t - 2) >> 1) & 1, ab, 1))) break;
+      uint8_t *bufp = smem + P::kB + buf * P::kBuf + off_blk;
+#pragma unroll
+      for (int i = 0; i < CPR; ++i) {
+        const int n = key0 + RPI * i;  // key within the tile
+        const bool live = kbase + n < s.nkv && ch_live;
+        float x[8];
+        unpack8<BF16>(raw[i], x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = live ? __fsub_rn(x[e], mu8[e]) : 0.f;
+        uint32_t w0[4], w1[4], w2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t a0, a1, a2, b0, b1, b2;
+          split3(x[2 * e], a0, a1, a2);
+          split3(x[2 * e + 1], b0, b1, b2);
+          w0[e] = a0 | (b0 << 16);
+          w1[e] = a1 | (b1 << 16);
+          w2[e] = a2 | (b2 << 16);
+        }
+        // 64 channels per 128-byte row; 16-byte chunk j of row n at position j ^ (n & 7)
+        uint8_t *dst = bufp + n * 128 + (((c8 & 7) ^ (n & 7)) << 4);
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        *reinterpret_cast<uint4 *>(dst + P::kPiece) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        *reinterpret_cast<uint4 *>(dst + 2 * P::kPiece) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+      }
+      fence_async_smem();  // the generic-proxy stores become visible to the MMA
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b_full[buf]);
+    }
+  } else if (warp < kDsMmaWarp) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    // the warp's largest visited tile: its last valid row has the largest Q block
+    const int r_last = min(nrows - 1, r0 + q * 32 + 31);
+    const int vis_warp = (r0 + q * 32 < nrows)
+                             ? (g.causal ? kv_tiles_for(r_last / grp, s.nq, s.nkv, 1) : ntile_kv)
+                             : 0;
+    // the staging block of this warp: 32 rows x 32 floats, 16-byte chunk j of row r at j ^ (r & 7)
+    float *stage = reinterpret_cast<float *>(smem + P::kStage) + q * 32 * 32;
+    // in the store phase lane l writes chunk l % 8 of rows 4 i + l / 8: their dsc rows
+    float *orow[8];
+    int ovis[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = r0 + q * 32 + 4 * i + lane / 8;
+      const bool ok_r = rr < nrows;
+      const int qb_r = ok_r ? rr / grp : 0, hq_r = hk * grp + (ok_r ? rr % grp : 0);
+      orow[i] = a.w.dsc + ((size_t)hq_r * a.L.nqblk + s.qpad0 / kBQ + qb_r) * a.L.nkv_pad;
+      ovis[i] = ok_r ? (g.causal ? kv_tiles_for(qb_r, s.nq, s.nkv, 1) : ntile_kv) : 0;
+    }
+    bool ok = true;
+#pragma unroll 1
+    for (int t = 0; t < nt && ok; ++t) {
+      const int buf = t & 1;
+      if (!(ok = ds_wait(&acc_full[buf], (t >> 1) & 1, ab, 2))) break;
+      tc_fence_after();
+      const int kt = t0 + t;
+      if (kt < vis_warp) {
+        const uint32_t tA = tbase + lane_base + kColAcc + buf * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32_wait(tA + 32 * c, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4 *>(stage + lane * 32 + ((j ^ (lane & 7)) << 2)) =
+                make_float4(__fmul_rn(__uint_as_float(v[4 * j]), g.c32),
+                            __fmul_rn(__uint_as_float(v[4 * j + 1]), g.c32),
+                            __fmul_rn(__uint_as_float(v[4 * j + 2]), g.c32),
+                            __fmul_rn(__uint_as_float(v[4 * j + 3]), g.c32));
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + lane / 8, j = lane & 7;
+            const float4 f = *reinterpret_cast<const float4 *>(stage + r * 32 + ((j ^ (r & 7)) << 2));
+            if (kt < ovis[i])
+              *reinterpret_cast<float4 *>(orow[i] + kt * kBKV + 32 * c + 4 * j) = f;
+          }
+          __syncwarp();  // the block is read before the next chunk overwrites it
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (one lane)
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+    // piece products, smallest first: (qmean piece, K~ piece), 0 = the leading piece
+    constexpr int kPa[6] = {2, 1, 0, 1, 0, 0}, kPb[6] = {0, 1, 2, 0, 1, 0};
+    bool ok = mbar_wait(a_full, 0, ab, 3);
+#pragma unroll 1
+    for (int t = 0; t < nt && ok; ++t) {
+      const int buf = t & 1;
+      ok = mbar_wait(&b_full[buf], (t >> 1) & 1, ab, 4) &&
+           (t < 2 || mbar_wait(&acc_empty[buf], ((t - 2) >> 1) & 1, ab, 5));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tbase + kColAcc + buf * 128;
+      const uint32_t bbase = smem_u32(smem + P::kB + buf * P::kBuf);
+#pragma unroll
+      for (int pp = 0; pp < 6; ++pp) {
+        const uint64_t bdesc = sdesc_kmajor(bbase + kPb[pp] * P::kPiece, 128);
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk)  // 16 channels = 32 bytes per MMA
+          mma_f16_ts(d, tbase + kColA + kPa[pp] * (DP / 2) + kk * 8,
+                     bdesc + (uint64_t)((kk & 3) * 2 + (kk >> 2) * (16384 >> 4)), idesc,
+                     (pp > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&b_empty[buf]);
+      mma_commit(&acc_full[buf]);
+    }
+    mma_commit(drain);  // every MMA issued above completes before tensor memory is freed
+    const uint64_t t_drain = global_timer_ns();
+    while (!mbar_try_wait(drain, 0))
+      if (global_timer_ns() - t_drain > SAGE2_WAIT_NS) break;
   }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kDsMmaWarp) tmem_dealloc(tbase, 512);
 }
 
 }  // namespace
@@ -716,15 +854,9 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   const dim3 stat_grid(L.nchunk, g.B, (nvec + stat_vpb - 1) / stat_vpb);
   const dim3 kv_grid(kv_tiles, g.Hkv, g.B);
   const dim3 q_grid(q_tiles, g.Hq, g.B);
-  // DeltaS row-tile height: the fewest computed rows for the (Q block, head) rows of a kv
-  // head, the taller tile on ties (more reuse of each staged key)
+  // DeltaS: 128-row tiles of (Q block, q head) pairs, kDsChunk key tiles per CTA
   const int max_rows = (g.Hq / g.Hkv) * q_tiles;
-  int ds_rows = 128;
-  for (int r : {64, 32})
-    if ((max_rows + r - 1) / r * r < (max_rows + ds_rows - 1) / ds_rows * ds_rows) ds_rows = r;
-  const int ds_keys = kBQ * kBKV / ds_rows;
-  const dim3 ds_grid((max(1, g.max_nkv) + ds_keys - 1) / ds_keys,
-                     (max_rows + ds_rows - 1) / ds_rows, g.B * g.Hkv);
+  const dim3 ds_grid((kv_tiles + kDsChunk - 1) / kDsChunk, (max_rows + 127) / 128, g.B * g.Hkv);
   // kernels instantiated per padded head dim and input type
   // kernels instantiated per padded head dim, input type and code grid. The INT8 path (the
   // SageAttention (v1) switch) has per-block scales, no Q smoothing and so no DeltaS: the
@@ -739,12 +871,15 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
     v_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
     q_quant<DP, BF, I8><<<q_grid, 256, 0, st>>>(a);
     if (I8) return;
-    if (ds_rows == 128)
-      delta_s<DP, 128, BF><<<ds_grid, 256, 0, st>>>(a);
-    else if (ds_rows == 64)
-      delta_s<DP, 64, BF><<<ds_grid, 256, 0, st>>>(a);
-    else
-      delta_s<DP, 32, BF><<<ds_grid, 256, 0, st>>>(a);
+    constexpr int kSmem = DsPlan<DP>::kBytes;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(delta_s_tc<DP, BF>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    });
+    if (attr_err != cudaSuccess) return;
+    delta_s_tc<DP, BF><<<ds_grid, kDsThreads, kSmem, st>>>(a);
   };
   auto run_dp = [&](auto i8_tag) {
     using T128 = std::integral_constant<int, 128>;

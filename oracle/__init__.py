@@ -211,7 +211,8 @@ def quant_v(v, dtype, cu_kv, Hkv, D0, vamax):
 
 
 def delta_s(k, dtype, cu_kv, b, Hkv, hk, D0, kmean, qbar):
-    """FP32 Delta-S = qbar . (K - kmean) for every key of sequence b, kv head hk."""
+    """Delta-S = qbar . fl32(K - kmean) for every key of sequence b, kv head hk: the FP64 dot
+    product of the FP32 operands rounded once to FP32."""
     k = _u16(k)
     ck = _cu(cu_kv)
     Dp = padded_dim(D0)

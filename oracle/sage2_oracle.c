@@ -485,22 +485,26 @@ void oracle_quant_v(const uint16_t *v, int dtype, int B, const int *cu_kv, int H
  * [P3] component 1). With K smoothed, K^T may be replaced by K~^T: the
  * difference qmean . kmean is the same for every key, and softmax rows do not
  * change under a per-row constant. Computed from the unquantized smoothed
- * K~ = fl32(K - kmean), in FP32 with one fused multiply-add per channel in
- * increasing channel order, because it feeds the e4m3 code of P~ [R]:
- *   acc = 0; for d: acc = fma(qmean[d], K~[j,d], acc).
+ * K~ = fl32(K - kmean) in full precision [R]: every product of two FP32
+ * values is exact in FP64 and the sum over the channels is carried in FP64,
+ * then rounded once to FP32, which gives the correctly rounded exact dot
+ * product unless it lies within about 2^-46 (relative) of an FP32 rounding
+ * midpoint. The e4m3 codes of P~ depend on it only through the rounding of
+ * 448 P: a Delta-S a few ulp away moves a code only where 448 P sits at a
+ * midpoint, the case the P~ comparisons already account for.
  * out[j] for the nkv keys of sequence b. */
 void oracle_delta_s(const uint16_t *k, int dtype, const int *cu_kv, int b, int Hkv, int hk, int D0,
                     int Dp, const float *kmean, const float *qbar, float *out) {
   const int n = cu_kv[b + 1] - cu_kv[b];
   const float *mu = kmean ? kmean + ((size_t)b * Hkv + hk) * Dp : NULL;
   for (int j = 0; j < n; j++) {
-    float acc = 0.f;
+    double acc = 0.0;
     for (int d = 0; d < D0; d++) {
       float x = (float)in_val(k, tix(cu_kv[b] + j, hk, Hkv, D0) + d, dtype);
-      if (mu) x = x - mu[d];
-      acc = fmaf(qbar[d], x, acc);
+      if (mu) x = x - mu[d]; /* K~ = fl32(K - kmean) */
+      acc += (double)qbar[d] * (double)x;
     }
-    out[j] = acc;
+    out[j] = (float)acc;
   }
 }
 

@@ -103,12 +103,10 @@ def mode_q(q, k, v, cu_q, cu_kv, hq, hkv, d0, causal, sm_scale=0.0, bq=128, bkv=
                     if smooth_q else np.zeros(d0, F32)
                 if per_block:
                     blk_codes, blk_scale = quantize_group((Q[r0:r0 + bq].astype(F32) - qbar).astype(F32), G)
-                dS = []
-                for j in range(nkv):
-                    acc = F32(0)
-                    for c in range(d0):
-                        acc = fma32(qbar[c], Kt[j, c], acc)
-                    dS.append(acc)
+                # Delta-S: the exact dot product of the FP32 operands (math.fsum of exact FP64
+                # products), rounded to FP32
+                dS = [F32(math.fsum(float(qbar[c]) * float(Kt[j, c]) for c in range(d0)))
+                      for j in range(nkv)]
                 for i in rows:
                     qt = (Q[i].astype(F32) - qbar).astype(F32)
                     qc, qs = (blk_codes[i - r0], blk_scale) if per_block else quantize_group(qt, G)

@@ -34,8 +34,8 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import (GpuCase, bits, c32_of, check_forward_proven, compare_p_codes, kv_tiles,
-                         metrics, pad_starts)
+from parity_util import (GpuCase, bits, c32_of, check_dsc, check_forward_proven, compare_p_codes,
+                         ds_abs_sum, kv_tiles, metrics, pad_starts)
 
 pytestmark = pytest.mark.gpu
 
@@ -122,11 +122,12 @@ def test_prepass_bit_exact_with_switches(name, setting):
             for qb in range(nqb):
                 blk = qp[b] // 128 + qb
                 np.testing.assert_array_equal(got["qmean"][h, blk], qmean[b, h, qb])
-                ds = oracle.delta_s(bits(x["k"]), dt, x["cu_kv"], b, w.hkv, h // (w.hq // w.hkv),
-                                    w.d, km, qmean[b, h, qb])
+                hk = h // (w.hq // w.hkv)
+                ds = oracle.delta_s(bits(x["k"]), dt, x["cu_kv"], b, w.hkv, hk, w.d, km,
+                                    qmean[b, h, qb])
                 n = min(w.nkv[b], kv_tiles(qb, w.nq[b], w.nkv[b], w.causal) * 128)
-                want = (ds[:n] * c32).astype(np.float32)
-                np.testing.assert_array_equal(got["dsc"][h, blk, :n], want)
+                check_dsc(got["dsc"][h, blk, :n], ds[:n],
+                          ds_abs_sum(x, w, b, hk, km, qmean[b, h, qb])[:n], c32)
 
 
 @pytest.mark.parametrize("setting", list(SETTINGS))

@@ -1,7 +1,8 @@
 """GPU parity: the CUDA path against the CPU oracle, through the C ABI.
 
 Gates (per the method's emulation, the oracle's Mode Q):
-  * prepass results (means, INT4 codes and scales, e4m3 V codes, DeltaS*c) bit-exact;
+  * prepass results (means, INT4 codes and scales, e4m3 V codes) bit-exact; DeltaS*c within
+    128 units of 2^-24 of c * sum |qmean K~| (plus 2 ulp) of the oracle's FP64 dot product;
   * the raw integer Q K^T accumulators of the tensor-core MMA bit-exact;
   * the output (FP32) within relative L1 1e-3 and max abs 2e-3;
   * fp16/bf16 outputs within one unit in the last place of the oracle's rounded output.
@@ -17,8 +18,8 @@ import torch
 import oracle
 import bit_exact_attention_gb300 as S
 from bit_exact_attention_gb300 import workloads as W
-from parity_util import (GpuCase, bits, c32_of, check_forward_proven, e4m3_to_f64, kv_tiles,
-                         metrics, pad_starts, unit_rows, units_sample)
+from parity_util import (GpuCase, bits, c32_of, check_dsc, check_forward_proven, ds_abs_sum,
+                         e4m3_to_f64, kv_tiles, metrics, pad_starts, unit_rows, units_sample)
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +68,7 @@ def run_case(name):
 
 # ------------------------------------------------------------------ prepass
 @pytest.mark.parametrize("name", list(SCALED))
-def test_prepass_bit_exact(name):
+def test_prepass_codes_bit_exact_delta_s_bounded(name):
     w, x, g = run_case(name)
     g.prepass()
     assert g.status() == (0, 0)
@@ -87,18 +88,21 @@ def test_prepass_bit_exact(name):
     # Q block means and DeltaS * c for every (q head, Q block, visited KV tile)
     qp, kp = pad_starts(x["cu_q"]), pad_starts(x["cu_kv"])
     c32 = c32_of(w)
+    worst = 0.0
     for b in range(w.batch):
         nqb = (w.nq[b] + 127) // 128
         for h in range(w.hq):
             for qb in range(nqb):
                 blk = qp[b] // 128 + qb
                 np.testing.assert_array_equal(got["qmean"][h, blk], qmean[b, h, qb])
-                ds = oracle.delta_s(bits(x["k"]), dt, x["cu_kv"], b, w.hkv, h // (w.hq // w.hkv),
-                                    w.d, kmean, qmean[b, h, qb])
+                hk = h // (w.hq // w.hkv)
+                ds = oracle.delta_s(bits(x["k"]), dt, x["cu_kv"], b, w.hkv, hk, w.d, kmean,
+                                    qmean[b, h, qb])
                 ntiles = kv_tiles(qb, w.nq[b], w.nkv[b], w.causal)
                 n = min(w.nkv[b], ntiles * 128)
-                want = (ds[:n] * c32).astype(np.float32)
-                np.testing.assert_array_equal(got["dsc"][h, blk, :n], want, err_msg=f"{b},{h},{qb}")
+                absum = ds_abs_sum(x, w, b, hk, kmean, qmean[b, h, qb])
+                worst = max(worst, check_dsc(got["dsc"][h, blk, :n], ds[:n], absum[:n], c32))
+    print(f"{name}: largest DeltaS*c deviation {worst:.3f} of its bound")
 
 
 # ------------------------------------------------------------------ integer accumulators
@@ -160,8 +164,7 @@ def test_forward_matches_emulation_fp32(name):
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle_ref(w, x)
-    m = metrics(out, emu)
-    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+    check_forward_proven(g, w, x, out, emu)
     ex = oracle_ref(w, x, mode="exact")
     mg, mq = metrics(out, ex), metrics(emu, ex)
     # the GPU is exactly as accurate as the method it implements
@@ -182,8 +185,7 @@ def test_one_tile_kernel_matches_emulation(name, monkeypatch):
     monkeypatch.setenv("SAGE2_ATTN_PP", "0")
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
-    m = metrics(out, oracle_ref(w, x))
-    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+    check_forward_proven(g, w, x, out, oracle_ref(w, x))
     m2 = metrics(default, out)
     scale = float(np.abs(out).max()) if out.size else 0.0
     assert m2["relL1"] <= 1e-6 and m2["maxabs"] <= 2.0 ** -18 * max(scale, 1e-30), m2
@@ -199,13 +201,12 @@ def test_forward_low_precision_output(name):
     want_bits = oracle.round_output(emu, W.dtype_code(w))
     want = torch.from_numpy(want_bits.view(np.int16)).view(x["q"].dtype).double().numpy()
     # The FP32 result may sit up to MAX_ABS from the emulation; rounding both to the
-    # output dtype adds at most one unit in the last place of the larger of the two.
+    # output dtype adds at most one unit in the last place of the larger of the two. Rows beyond
+    # that must be explained by located P~ midpoint flips (check_forward_proven).
     mant = 7 if w.dtype == "bf16" else 10
     mag = np.maximum(np.abs(want), np.abs(got))
     ulp = np.exp2(np.floor(np.log2(np.maximum(mag, 1e-30))) - mant)
-    excess = np.abs(got - want) - (MAX_ABS + ulp)
-    assert excess.max() <= 0, f"{int((excess > 0).sum())} elements beyond MAX_ABS + 1 ulp"
-    assert metrics(got, want)["relL1"] <= REL_L1
+    check_forward_proven(g, w, x, got, want, tol=MAX_ABS + ulp)
 
 
 def test_dense_entry_point_equals_varlen():
@@ -256,11 +257,10 @@ def test_edge_cases(case, kernel, monkeypatch):
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     assert g.status() == (0, 0)
     emu = oracle_ref(w, x)
-    m = metrics(out, emu)
     if np.abs(emu).sum() == 0:
         assert np.all(out == 0)
     else:
-        assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+        check_forward_proven(g, w, x, out, emu)
     # rows with no visible key are exactly zero
     for b in range(w.batch):
         for i in range(w.nq[b]):
@@ -316,8 +316,7 @@ def test_sm_scale_argument():
     out = g.forward(out_dtype=torch.float32).cpu().numpy()
     emu = oracle.attention_emulated(bits(x["q"]), bits(x["k"]), bits(x["v"]), 0, x["cu_q"],
                                     x["cu_kv"], 2, 2, 64, False, 0.05)
-    m = metrics(out, emu)
-    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+    check_forward_proven(g, w, x, out, emu)
 
 
 # ------------------------------------------------------------------ full-size workloads
@@ -334,9 +333,7 @@ def test_full_size_sampled_units(wl):
     units = units_sample(wl, 32, seed=wl.seed)
     emu = oracle_ref(wl, x, units=units)
     toks, heads = unit_rows(wl, x["cu_q"], units)
-    got = out[torch.from_numpy(toks).cuda(), torch.from_numpy(heads).cuda()].cpu().numpy()
-    m = metrics(got, emu[toks, heads])
-    assert m["relL1"] <= REL_L1 and m["maxabs"] <= MAX_ABS, m
+    check_forward_proven(g, wl, x, out.cpu().numpy(), emu, rows=(toks, heads))
 
 
 @pytest.mark.parametrize("wl", [W.PREFILL, W.VARLEN], ids=["prefill", "varlen"])
