@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
 //        for the key tiles each row's Q block visits;
 //   12   MMA issuer (one lane); it also allocates tensor memory.
 // Tensor memory: the qmean pieces at [0, 3 DP / 2), two 128-column accumulators at 256 and 384.
-constexpr int kDsChunk = 8;  // key tiles per CTA
+constexpr int kDsChunk = 16;  // key tiles per CTA
 constexpr int kDsThreads = 416, kDsLoadWarps = 8, kDsMmaWarp = 12;  // epilogue: warps 8-11
 
 template <int DP>
