@@ -207,26 +207,36 @@ __device__ __forceinline__ float logits128(float2 (&x)[64], const uint32_t (&v)[
 
 // P448 = 2^(S' - m448) for the 128 keys of a row (masked keys give 0), their sum (pairs summed
 // into four accumulators by pair index mod 4, then combined in a fixed order) and the e4m3 codes
-// P~ = e4m3(P448), key 4e + i in byte i of pk[e].
-__device__ __forceinline__ float probs128(float2 (&x)[64], float m448, uint32_t (&pk)[32]) {
+// P~ = e4m3(P448), key 4e + i in byte i of pk[e]. The codes of each 32-key chunk are stored to
+// the row's P~ buffer `prow` (16-byte piece c at position c ^ (row & 7), the 128-byte swizzle)
+// as soon as they exist, so the stores drain while the next chunk's exponentials run.
+__device__ __forceinline__ float probs128(float2 (&x)[64], float m448, uint32_t (&pk)[32],
+                                          uint8_t *prow, int row) {
   const float2 nm = make_float2(-m448, -m448);
-#pragma unroll
-  for (int k = 0; k < 64; ++k) {
-    x[k] = __fadd2_rn(x[k], nm);
-    x[k].x = ex2_approx(x[k].x);
-    x[k].y = ex2_approx(x[k].y);
-  }
   float2 ps[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) ps[q] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < 64; ++k) ps[k & 3] = __fadd2_rn(ps[k & 3], x[k]);
-  const float rs = __fadd_rn(__fadd_rn(__fadd_rn(ps[0].x, ps[0].y), __fadd_rn(ps[1].x, ps[1].y)),
-                             __fadd_rn(__fadd_rn(ps[2].x, ps[2].y), __fadd_rn(ps[3].x, ps[3].y)));
+  for (int c = 0; c < 4; ++c) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e)
-    pk[e] = cvt_e4m3x4(x[2 * e].x, x[2 * e].y, x[2 * e + 1].x, x[2 * e + 1].y);
-  return rs;
+    for (int k = 16 * c; k < 16 * c + 16; ++k) {
+      x[k] = __fadd2_rn(x[k], nm);
+      x[k].x = ex2_approx(x[k].x);
+      x[k].y = ex2_approx(x[k].y);
+    }
+#pragma unroll
+    for (int k = 16 * c; k < 16 * c + 16; ++k) ps[k & 3] = __fadd2_rn(ps[k & 3], x[k]);
+#pragma unroll
+    for (int e = 8 * c; e < 8 * c + 8; ++e)
+      pk[e] = cvt_e4m3x4(x[2 * e].x, x[2 * e].y, x[2 * e + 1].x, x[2 * e + 1].y);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      *reinterpret_cast<uint4 *>(prow + (((2 * c + h) ^ (row & 7)) << 4)) =
+          make_uint4(pk[8 * c + 4 * h], pk[8 * c + 4 * h + 1], pk[8 * c + 4 * h + 2],
+                     pk[8 * c + 4 * h + 3]);
+  }
+  return __fadd_rn(__fadd_rn(__fadd_rn(ps[0].x, ps[0].y), __fadd_rn(ps[1].x, ps[1].y)),
+                   __fadd_rn(__fadd_rn(ps[2].x, ps[2].y), __fadd_rn(ps[3].x, ps[3].y)));
 }
 
 // End of every role branch: all 512 threads meet once more (each warp from its own branch, so
@@ -662,12 +672,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // maximum of the warp moved, it waits for PV_t(j-1) and rescales O_t by alpha(j) in tensor memory.
 // It writes P~_t(j) into buffer j % 2 (free: QK_t(j) is issued only after PV_t(j-2) completed)
 // and hands it to the P~V issuer; PV_t(j) then adds the block partial P~(j) V(j) into O_t.
-// The two issuers are event driven and independent of each other. Issuing a group of MMAs blocks
-// the issuing thread while the tensor pipe is busy (a few hundred cycles per group); with one
-// thread for both products, each P~V issue delayed the next Q K^T of both tiles by that much, and
-// the softmax waited for S. tcgen05.commit covers the MMAs of the issuing thread only, so each
-// issuer signals its own products: s_full_t after QK_t(n), pv_done[t][n % 2] after PV_t(n), and
-// one arrival each on a stage's empty barrier once all its products reading the stage are issued.
+// The two issuers are separate threads: issuing a group of MMAs blocks the issuing thread while
+// the tensor pipe is busy (a few hundred cycles per group), and with one thread for both
+// products each P~V issue delayed the next Q K^T of both tiles by that much. Each follows a fixed
+// order (n = 0, 1, ..., tile 0 then tile 1) with blocking waits: polling several barriers in turn
+// kept the issuer's sub-partition busy and slowed the softmax warps sharing it, which paced the
+// whole CTA. tcgen05.commit covers the MMAs of the issuing thread only, so each issuer signals its
+// own products: s_full_t after QK_t(n), pv_done[t][n % 2] after PV_t(n), and one arrival each on
+// a stage's empty barrier once all its products reading the stage complete.
 template <int DP, int ST>
 struct PPPlan {
   static constexpr int kQ = 0;                       // [2][128 rows][DP]   (swizzled)
@@ -685,7 +697,7 @@ struct PPPlan {
   static constexpr int kBytes = kEnd + 1024;
   static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
-// register split: the control warpgroup keeps 56 (its event loops spill at 40), the two softmax
+// register split: the control warpgroup keeps 56 (its loops spilled at 40), the two softmax
 // warpgroups take 224 each (56 + 2 x 224 = 3 x 168, the launch budget)
 constexpr int kPPRegsCtl = 56, kPPRegsSoftmax = 224;
 static_assert(kPPRegsCtl + 2 * kPPRegsSoftmax <= 3 * kRegsLaunch, "register split above budget");
@@ -693,29 +705,6 @@ static_assert(kPvWarp != 3, "warp 3 stages the V channel scales");
 // tensor-memory columns of tile t: S at 256 t, O at 256 t + 128
 __device__ __forceinline__ uint32_t pp_col_s(int t) { return (uint32_t)t * 256u; }
 __device__ __forceinline__ uint32_t pp_col_o(int t) { return (uint32_t)t * 256u + 128u; }
-
-// Idle bookkeeping of an event-driven issuer: after SAGE2_WAIT_NS of global time without
-// progress (or once another warp gave up) it gives up too, recording `site`.
-struct IdleClock {
-  uint64_t t_idle = 0;  // global time when the current idle spell was first checked
-  uint32_t idle = 0;    // polls without progress (the clock is read every 64th)
-  __device__ __forceinline__ bool step(bool progress, const AbortCtx &ab, int site) {
-    if (progress) {
-      idle = 0;
-      return true;
-    }
-    if ((++idle & 63u) != 0) return true;
-    const uint64_t now = global_timer_ns();
-    if (idle == 64) t_idle = now;
-    if (*ab.flag) return false;
-    if (now - t_idle > SAGE2_WAIT_NS) {
-      *ab.flag = 1;
-      if (ab.status) atomicCAS(ab.status, 0, kStatusTimeoutBase | site);
-      return false;
-    }
-    return true;
-  }
-};
 
 // One 128-row tile's output rows from the FP32 accumulator in tensor memory: O * vscale / l,
 // rounded to the output type (row `row` of the tile, `o` its element offset in the output).
@@ -893,83 +882,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- Q K^T issuer (one lane)
-      // QK_t(n) once K(n) has landed, the softmax of tile t has read S_t(n-1) and PV_t(n-2) is
-      // complete: the softmax then knows from s_full_t(n) alone that P~ buffer n % 2 is free. This
-      // thread tests every phase of pv_done[t][b] in order, so the softmax's own parity waits on
-      // those barriers (PV_t(j-1) for a rescale, PV_t(T-1) for the epilogue) come at most one
-      // phase ahead of what has been seen complete. Stage n is released (this issuer's arrival)
-      // once QK_0(n) and QK_1(n) have been issued.
+      // In the fixed order n = 0, 1, ..., tile 0 then tile 1, each with blocking waits: QK_t(n)
+      // once the softmax of tile t has read S_t(n-1), PV_t(n-2) is complete (so the softmax
+      // knows from s_full_t(n) alone that P~ buffer n % 2 is free, and its own parity waits on
+      // pv_done come at most one phase ahead of what has completed) and K(n) has landed. Stage n
+      // gets this issuer's arrival once QK_0(n) and QK_1(n) complete.
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
       bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
-      int nq0 = 0, nq1 = 0, ne = 0;
-      IdleClock clk;
-      while (ok && (nq0 < T0 || nq1 < T1)) {
-        bool progress = false;
+      for (int n = 0; ok && n < Tmax; ++n) {
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          int &nq = t ? nq1 : nq0;
-          const int T = t ? T1 : T0;
-          if (nq < T && (nq == 0 || mbar_test_wait(&s_free[t], (nq - 1) & 1)) &&
-              (nq < 2 || mbar_test_wait(&pv_done[2 * t + (nq & 1)], ((nq - 2) >> 1) & 1)) &&
-              mbar_test_wait(&kv_full[nq % ST], (nq / ST) & 1)) {
-            tc_fence_after();
-            const uint64_t adesc = sdesc_kmajor(smem_u32(smem + P::kQ + t * 128 * DP), DP);
-            const uint64_t kdesc =
-                sdesc_kmajor(smem_u32(smem + P::kK + (nq % ST) * 128 * DP), DP);
+          if (!ok || n >= (t ? T1 : T0)) continue;
+          if (n > 0) ok = mbar_wait(&s_free[t], (n - 1) & 1, ab, kSiteSFree);
+          if (ok && n >= 2)
+            ok = mbar_wait(&pv_done[2 * t + (n & 1)], ((n - 2) >> 1) & 1, ab, kSitePvDone);
+          if (ok) ok = mbar_wait(&kv_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t adesc = sdesc_kmajor(smem_u32(smem + P::kQ + t * 128 * DP), DP);
+          const uint64_t kdesc = sdesc_kmajor(smem_u32(smem + P::kK + (n % ST) * 128 * DP), DP);
 #pragma unroll
-            for (int kk = 0; kk < DP / 32; ++kk)
-              mma_e4m3_ss(tbase + pp_col_s(t), adesc + (uint64_t)(kk * 2),
-                          kdesc + (uint64_t)(kk * 2), idesc_qk, kk > 0);
-            mma_commit(&s_full[t]);
-            ++nq;
-            progress = true;
-            while (ne < Tmax && (ne >= T0 || nq0 > ne) && (ne >= T1 || nq1 > ne)) {
-              mma_commit(&kv_empty[ne % ST]);
-              ++ne;
-            }
-          }
+          for (int kk = 0; kk < DP / 32; ++kk)
+            mma_e4m3_ss(tbase + pp_col_s(t), adesc + (uint64_t)(kk * 2),
+                        kdesc + (uint64_t)(kk * 2), idesc_qk, kk > 0);
+          mma_commit(&s_full[t]);
         }
-        ok = clk.step(progress, ab, kSiteSFree);
+        if (ok) mma_commit(&kv_empty[n % ST]);
       }
       mma_commit(&drain[0]);  // every MMA issued above completes before tensor memory is freed
       drain_wait(&drain[0], 0);
     } else if (warp == kPvWarp && lane == 0) {
       // ---------------------------------------------------------- P~V issuer (one lane)
-      // PV_t(n) once P~_t(n) is written (after the rescale of O_t); stage n is released (this
-      // issuer's arrival) once PV_0(n) and PV_1(n) have been issued. The kv_full test is already
-      // complete when P~_t(n) exists (QK_t(n) waited for it); it orders the V reads after the
-      // copy for this thread too.
+      // Same order: PV_t(n) once P~_t(n) is written (after the rescale of O_t). The kv_full test
+      // is already complete when P~_t(n) exists (QK_t(n) waited for it); it orders the V reads
+      // after the copy for this thread too. Stage n gets this issuer's arrival once PV_0(n) and
+      // PV_1(n) complete.
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
       bool ok = true;
-      int np0 = 0, np1 = 0, ne = 0;
-      IdleClock clk;
-      while (ok && (np0 < T0 || np1 < T1)) {
-        bool progress = false;
+      for (int n = 0; ok && n < Tmax; ++n) {
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          int &np = t ? np1 : np0;
-          const int T = t ? T1 : T0;
-          if (np < T && mbar_test_wait(&p_full[2 * t + (np & 1)], (np >> 1) & 1) &&
-              mbar_test_wait(&kv_full[np % ST], (np / ST) & 1)) {
-            tc_fence_after();
-            const uint64_t pdesc =
-                sdesc_kmajor(smem_u32(smem + P::kP + (2 * t + (np & 1)) * 16384), 128);
-            const uint64_t vdesc =
-                sdesc_kmajor(smem_u32(smem + P::kV + (np % ST) * DP * 128), 128);
+          if (!ok || n >= (t ? T1 : T0)) continue;
+          ok = mbar_wait(&p_full[2 * t + (n & 1)], (n >> 1) & 1, ab, kSitePFull);
+          if (ok) ok = mbar_wait(&kv_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t pdesc =
+              sdesc_kmajor(smem_u32(smem + P::kP + (2 * t + (n & 1)) * 16384), 128);
+          const uint64_t vdesc = sdesc_kmajor(smem_u32(smem + P::kV + (n % ST) * DP * 128), 128);
 #pragma unroll
-            for (int kk = 0; kk < kBKV / 32; ++kk)
-              mma_e4m3_ss(tbase + pp_col_o(t), pdesc + (uint64_t)(kk * 2),
-                          vdesc + (uint64_t)(kk * 2), idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&pv_done[2 * t + (np & 1)]);
-            ++np;
-            progress = true;
-            while (ne < Tmax && (ne >= T0 || np0 > ne) && (ne >= T1 || np1 > ne)) {
-              mma_commit(&kv_empty[ne % ST]);
-              ++ne;
-            }
-          }
+          for (int kk = 0; kk < kBKV / 32; ++kk)
+            mma_e4m3_ss(tbase + pp_col_o(t), pdesc + (uint64_t)(kk * 2),
+                        vdesc + (uint64_t)(kk * 2), idesc_pv, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&pv_done[2 * t + (n & 1)]);
         }
-        ok = clk.step(progress, ab, kSitePFull);
+        if (ok) mma_commit(&kv_empty[n % ST]);
       }
       mma_commit(&drain[1]);
       drain_wait(&drain[1], 0);
@@ -1037,16 +1004,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool none = (m_new == -INFINITY);
         const float alpha = none ? 1.f : ex2_approx(__fsub_rn(m, m_new));
         const float m448 = none ? 0.f : __fsub_rn(m_new, L32);
+        // P~_t(j) into buffer j % 2, free: QK_t(j) was issued after PV_t(j-2) had completed
         uint32_t pk[32];
-        const float rs = probs128(x, m448, pk);
+        const float rs = probs128(x, m448, pk, prow0 + (j & 1) * 16384, row);
+        fence_async_smem();  // the generic-proxy stores become visible to the MMA
         if (dump) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             *reinterpret_cast<uint32_t *>(a.dbg.p_out + row * 128 + 4 * e) = pk[e];
         }
         // O = alpha O once PV_t(j-1) is complete (with every alpha of the warp's rows equal to 1
-        // there is nothing to do). P~ buffer j % 2 is free: QK_t(j) was issued after PV_t(j-2)
-        // had completed.
+        // there is nothing to do), while the P~ stores drain.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           ok = warp_all(
               mbar_wait(&pv_done[2 * t + ((j - 1) & 1)], ((j - 1) >> 1) & 1, ab, kSitePvDone));
@@ -1072,12 +1040,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st_wait();
         }
-        uint8_t *prow = prow0 + (j & 1) * 16384;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        fence_async_smem();  // the generic-proxy stores become visible to the MMA
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[2 * t + (j & 1)]);

@@ -1,7 +1,7 @@
 """CPU models of the attention kernels' synchronisation (bit_exact_attention_gb300/csrc/
 sage2_attention.cu). For attn_pp, the two-tile kernel, the model has a producer, a Q K^T issuer
-and a P~V issuer (separate threads, so separate in-order pipes whose commits track only their own
-MMAs), and the softmax warps of both tiles. For attn_fwd, the one-tile kernel, it has two issuers
+and a P~V issuer (separate threads with blocking waits in a fixed order, so separate in-order
+pipes whose commits track only their own MMAs), and the softmax warps of both tiles. For attn_fwd, the one-tile kernel, it has two issuers
 with their own pipes, softmax and fold warps, a 4-slot alpha ring and double-buffered P~ and R.
 In both, the agents meet on mbarriers that are waited on by phase parity, as the hardware does.
 
@@ -49,10 +49,11 @@ class Bar:
 
 
 class Model:
-    """attn_pp's protocol. QK_t(n) is issued once the softmax read S_t(n-1), K(n) landed and
-    PV_t(n-2) completed; PV_t(n) once P~_t(n) is written; each issuer gives a stage its own
-    arrival once all its products reading the stage are issued. pv_done[t][b] completes for the
-    PVs of P~ buffer b. The softmax rescales O_t after waiting for PV_t(j-1)."""
+    """attn_pp's protocol. Both issuers take n = 0, 1, ..., tile 0 then tile 1, with blocking
+    waits. QK_t(n) is issued once the softmax read S_t(n-1), PV_t(n-2) completed and K(n) landed;
+    PV_t(n) once P~_t(n) is written; each issuer gives stage n its own arrival (a commit, so once
+    its products reading the stage complete). pv_done[t][b] completes for the PVs of P~ buffer b.
+    The softmax stores P~_t(j), rescales O_t after waiting for PV_t(j-1), then hands P~ over."""
 
     def __init__(self, T0, T1, ST, W, rng, resc_p, qk_after_pv=True, pv_bar_per_buffer=True):
         self.T, self.ST, self.W, self.rng = (T0, T1), ST, W, rng
@@ -111,57 +112,36 @@ class Model:
             self.stage_users[j] = users
             yield ("act", self.kv_full[s].arrive)
 
-    def release(self, ne, done, pipe):
-        while ne < self.Tmax and (ne >= self.T[0] or done[0] > ne) and \
-                (ne >= self.T[1] or done[1] > ne):
-            self.pipes[pipe].append(("commit", self.kv_empty[ne % self.ST]))
-            ne += 1
-        return ne
-
     def qk_issuer(self):
-        nq, ne = [0, 0], 0
-        while nq[0] < self.T[0] or nq[1] < self.T[1]:
-            progress, start = False, self.events
+        """Fixed order n = 0, 1, ..., tile 0 then tile 1, each condition a blocking wait."""
+        for n in range(self.Tmax):
             for t in range(2):
-                n = nq[t]
                 if n >= self.T[t]:
                     continue
-                ok = n == 0 or self.s_free[t].passes(n - 1)
-                if ok and self.qk_after_pv and n >= 2:
-                    yield ("poll", True)  # a separate test: other agents move in between
-                    ok = self.pv_wait(t, n - 2)[0].passes(self.pv_wait(t, n - 2)[1])
-                if ok:
-                    yield ("poll", True)
-                    ok = self.kv_full[n % self.ST].passes(n // self.ST)
-                if ok:
-                    if n > 0 and min(self.s_read[t]) < n - 1:
-                        raise Hazard(f"QK{t}({n}) issued before S{t}({n - 1}) was read")
-                    self.pipes["qk"] += [("QK", t, n), ("commit", self.s_full[t])]
-                    nq[t] += 1
-                    progress = True
-                    ne = self.release(ne, nq, "qk")
-            yield ("poll", progress or self.events != start)
+                if n > 0:
+                    yield ("wait", self.s_free[t], n - 1)
+                if self.qk_after_pv and n >= 2:
+                    yield ("wait", *self.pv_wait(t, n - 2))
+                yield ("wait", self.kv_full[n % self.ST], n // self.ST)
+                if n > 0 and min(self.s_read[t]) < n - 1:
+                    raise Hazard(f"QK{t}({n}) issued before S{t}({n - 1}) was read")
+                self.pipes["qk"] += [("QK", t, n), ("commit", self.s_full[t])]
+            self.pipes["qk"].append(("commit", self.kv_empty[n % self.ST]))
 
     def pv_issuer(self):
-        np_, ne = [0, 0], 0
-        while np_[0] < self.T[0] or np_[1] < self.T[1]:
-            progress, start = False, self.events
+        for n in range(self.Tmax):
             for t in range(2):
-                n = np_[t]
-                if n < self.T[t] and self.p_full[t][n & 1].passes(n >> 1):
-                    yield ("poll", True)
-                    if not self.kv_full[n % self.ST].passes(n // self.ST):
-                        continue
-                    for w in range(self.W):
-                        if self.P[t][n & 1][w] != n:
-                            raise Hazard(f"PV{t}({n}) issued but warp {w}'s P~ buffer holds "
-                                         f"{self.P[t][n & 1][w]}")
-                    bar, _ = self.pv_wait(t, n)
-                    self.pipes["pv"] += [("PV", t, n), ("commit", bar)]
-                    np_[t] += 1
-                    progress = True
-                    ne = self.release(ne, np_, "pv")
-            yield ("poll", progress or self.events != start)
+                if n >= self.T[t]:
+                    continue
+                yield ("wait", self.p_full[t][n & 1], n >> 1)
+                yield ("wait", self.kv_full[n % self.ST], n // self.ST)
+                for w in range(self.W):
+                    if self.P[t][n & 1][w] != n:
+                        raise Hazard(f"PV{t}({n}) issued but warp {w}'s P~ buffer holds "
+                                     f"{self.P[t][n & 1][w]}")
+                bar, _ = self.pv_wait(t, n)
+                self.pipes["pv"] += [("PV", t, n), ("commit", bar)]
+            self.pipes["pv"].append(("commit", self.kv_empty[n % self.ST]))
 
     def pipe_step(self, name):
         kind = self.pipes[name].pop(0)
@@ -190,15 +170,17 @@ class Model:
             yield ("act", self.s_free[t].arrive)
             self.use_stage(j, f"softmax{t}.{w} DeltaS({j})")  # landed: QK_t(j) waited for it
             self.release_stage_user(j, ("SM", t, w))
+            # P~_t(j) is stored while the exponentials run, before the rescale
+            if self.pv_completed[t] < j - 1:
+                raise Hazard(f"softmax{t}.{w} overwrites P~ buffer {j & 1} before PV{t}({j - 2})")
+            self.P[t][j & 1][w] = j
+            yield ("act", lambda: None)
             if j > 0 and self.rng.random() < self.resc_p:
                 bar, ph = self.pv_wait(t, j - 1)
                 yield ("wait", bar, ph)
                 if self.pv_completed[t] != j:
                     raise Hazard(f"softmax{t}.{w} rescales O{t} at {j} with "
                                  f"{self.pv_completed[t]} PVs complete")
-            if self.pv_completed[t] < j - 1:
-                raise Hazard(f"softmax{t}.{w} overwrites P~ buffer {j & 1} before PV{t}({j - 2})")
-            self.P[t][j & 1][w] = j
             yield ("act", self.p_full[t][j & 1].arrive)
         if T > 0:
             bar, ph = self.pv_wait(t, T - 1)
