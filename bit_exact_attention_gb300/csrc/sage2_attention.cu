@@ -700,6 +700,9 @@ struct PPPlan {
 // register split: the control warpgroup keeps 56 (its loops spilled at 40), the two softmax
 // warpgroups take 224 each (56 + 2 x 224 = 3 x 168, the launch budget)
 constexpr int kPPRegsCtl = 56, kPPRegsSoftmax = 224;
+// sleep between barrier tests of the producer and the two issuers (measured best on the long
+// GQA workload; the producer's waits were the most sensitive: 1000 ns cost 7 %)
+constexpr uint32_t kPollProducerNs = 64, kPollQkNs = 64, kPollPvNs = 100;
 static_assert(kPPRegsCtl + 2 * kPPRegsSoftmax <= 3 * kRegsLaunch, "register split above budget");
 static_assert(kPvWarp != 3, "warp 3 stages the V channel scales");
 // tensor-memory columns of tile t: S at 256 t, O at 256 t + 128
@@ -862,7 +865,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < Tmax; ++j) {
         const int st = j % ST;
-        if (j >= ST && !mbar_wait<true>(&kv_empty[st], ((j / ST) - 1) & 1, ab, kSiteKvEmpty)) break;
+        if (j >= ST && !mbar_wait_poll<kPollProducerNs>(&kv_empty[st], ((j / ST) - 1) & 1, ab,
+                                                         kSiteKvEmpty))
+          break;
         const bool u0 = j < T0, u1 = j < T1;
         mbar_arrive_expect_tx(&kv_full[st],
                               128 * DP + DP * 128 + ((u0 ? 1 : 0) + (u1 ? 1 : 0)) * 512 + 16);
@@ -893,9 +898,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || n >= (t ? T1 : T0)) continue;
-          if (n > 0) ok = mbar_wait(&s_free[t], (n - 1) & 1, ab, kSiteSFree);
+          if (n > 0) ok = mbar_wait_poll<kPollQkNs>(&s_free[t], (n - 1) & 1, ab, kSiteSFree);
           if (ok && n >= 2)
-            ok = mbar_wait(&pv_done[2 * t + (n & 1)], ((n - 2) >> 1) & 1, ab, kSitePvDone);
+            ok = mbar_wait_poll<kPollQkNs>(&pv_done[2 * t + (n & 1)], ((n - 2) >> 1) & 1, ab,
+                                           kSitePvDone);
           if (ok) ok = mbar_wait(&kv_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
           if (!ok) break;
           tc_fence_after();
@@ -923,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || n >= (t ? T1 : T0)) continue;
-          ok = mbar_wait(&p_full[2 * t + (n & 1)], (n >> 1) & 1, ab, kSitePFull);
+          ok = mbar_wait_poll<kPollPvNs>(&p_full[2 * t + (n & 1)], (n >> 1) & 1, ab, kSitePFull);
           if (ok) ok = mbar_wait(&kv_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
           if (!ok) break;
           tc_fence_after();
@@ -976,11 +982,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t *prow0 = smem + P::kP + 2 * t * 16384 + row * 128;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
+      // Barrier phases are tested ahead of the blocking waits, at phase boundaries where the
+      // test's shared-memory round trip overlaps arithmetic: S_t(j+1) right after the P~ stores
+      // and their fence, PV_t(j-1) right after the logits. A wait then runs only if its test
+      // failed.
+      bool s_ready = false;
 #pragma unroll 1
       for (int j = 0; j < T; ++j) {
         const int st = j % ST;
-        ok = warp_all(mbar_wait(&s_full[t], j & 1, ab, kSiteSFull));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, s_ready)) {
+          ok = warp_all(mbar_wait(&s_full[t], j & 1, ab, kSiteSFull));
+          if (!ok) break;
+        }
         tc_fence_after();
         uint32_t v[128];
         tmem_ld128_nowait(tS, v);
@@ -1000,6 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = last_key - j * kBKV;
         float2 x[64];
         const float pmax = logits128(x, v, dsc, skv, sqc, lim);
+        const bool pv_ready =
+            j == 0 || mbar_test_wait(&pv_done[2 * t + ((j - 1) & 1)], ((j - 1) >> 1) & 1);
         const float m_new = fmaxf(m, pmax);
         const bool none = (m_new == -INFINITY);
         const float alpha = none ? 1.f : ex2_approx(__fsub_rn(m, m_new));
@@ -1008,6 +1023,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[32];
         const float rs = probs128(x, m448, pk, prow0 + (j & 1) * 16384, row);
         fence_async_smem();  // the generic-proxy stores become visible to the MMA
+        s_ready = j + 1 < T && mbar_test_wait(&s_full[t], (j + 1) & 1);
         if (dump) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
@@ -1016,9 +1032,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O = alpha O once PV_t(j-1) is complete (with every alpha of the warp's rows equal to 1
         // there is nothing to do), while the P~ stores drain.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          ok = warp_all(
-              mbar_wait(&pv_done[2 * t + ((j - 1) & 1)], ((j - 1) >> 1) & 1, ab, kSitePvDone));
-          if (!ok) break;
+          if (!__all_sync(0xffffffffu, pv_ready)) {
+            ok = warp_all(
+                mbar_wait(&pv_done[2 * t + ((j - 1) & 1)], ((j - 1) >> 1) & 1, ab, kSitePvDone));
+            if (!ok) break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int h = 0; h < DP / 64; ++h) {  // 64 columns per load

@@ -129,6 +129,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortC
   return mbar_wait_slow<LAZY>(bar, parity, ab, site);
 }
 
+// The same wait made of non-blocking tests with a sleep of NS nanoseconds between them. For the
+// producer and issuer threads that share a sub-partition with softmax warps: a thread spinning
+// on try_wait, or suspended in one, slowed those warps' shared-memory and MUFU work measurably,
+// and a sleeping poller costs them almost nothing (at the price of up to NS of wake-up delay).
+template <uint32_t NS>
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t *bar, uint32_t parity, AbortCtx ab,
+                                               int site) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(NS);
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*ab.flag) return false;
+    if (global_timer_ns() - t0 > SAGE2_WAIT_NS) {
+      *ab.flag = 1;
+      if (ab.status) atomicCAS(ab.status, 0, kStatusTimeoutBase | site);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA / bulk copies
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
