@@ -660,11 +660,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- two-tile kernel
-// One CTA per (sequence, q head, pair of 128-row Q tiles); the two tiles share every K/V stage,
-// so each K/V byte brought in feeds twice the tensor work. Warps: 0 TMA producer, 1 Q K^T issuer,
-// 2 P~V issuer, 3 stages the V channel scales, 4-7 softmax + epilogue of tile 0, 8-11 of tile 1
-// (each SM sub-partition runs one softmax warp of each tile, so one tile's arithmetic fills the
-// other's waits).
+// One CTA per (sequence, q head, pair of 128-row Q tiles); the two tiles share every K and V
+// stage, so each K/V byte brought in feeds twice the tensor work. Warps: 0 loads Q, K and the
+// DeltaS*c / K-scale ring, 1 Q K^T issuer, 2 P~V issuer, 3 stages the V channel scales and then
+// loads V, 4-7 softmax + epilogue of tile 0, 8-11 of tile 1 (each SM sub-partition runs one
+// softmax warp of each tile, so one tile's arithmetic fills the other's waits).
+// Three rings with their own barriers: K stage n is free once QK_0(n) and QK_1(n) complete, so
+// the next K tiles load well ahead; V stage n and DeltaS*c / K-scale stage n (read by the
+// softmax) once PV_0(n) and PV_1(n) complete. With one ring for all of them a stage stayed
+// held until the P~V products, and the K load of tile n + ST sat on the critical path.
 // Per tile t: tensor memory S_t [256 t, 256 t + 128) and O_t [256 t + 128, 256 t + 128 + DP) (the
 // FP32 output accumulator); Q_t codes and two P~_t buffers (128 x 128 e4m3, the A operand of
 // P~V) in shared memory, 128-byte swizzled K-major. Per KV tile j the softmax loads S_t(j) into
@@ -678,20 +682,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // order (n = 0, 1, ..., tile 0 then tile 1) with blocking waits: polling several barriers in turn
 // kept the issuer's sub-partition busy and slowed the softmax warps sharing it, which paced the
 // whole CTA. tcgen05.commit covers the MMAs of the issuing thread only, so each issuer signals its
-// own products: s_full_t after QK_t(n), pv_done[t][n % 2] after PV_t(n), and one arrival each on
-// a stage's empty barrier once all its products reading the stage complete.
+// own products: s_full_t after QK_t(n), pv_done[t][n % 2] after PV_t(n), k_empty(n) after the
+// two QK(n), v_empty(n) and d_empty(n) after the two PV(n).
 template <int DP, int ST>
 struct PPPlan {
   static constexpr int kQ = 0;                       // [2][128 rows][DP]   (swizzled)
   static constexpr int kP = kQ + 2 * 128 * DP;       // [2 tiles][2][128][128] (128B swizzled)
   static constexpr int kK = kP + 4 * 128 * 128;      // [ST][128 keys][DP]  (swizzled)
   static constexpr int kV = kK + ST * 128 * DP;      // [ST][DP][128 keys]  (swizzled)
-  static constexpr int kDsc = kV + ST * DP * 128;    // float [ST][2][128]
-  static constexpr int kSk = kDsc + ST * 2 * 512;    // float [ST][4]
-  static constexpr int kSv = kSk + ST * 16;          // float [DP]
+  static constexpr int kDS = 4;                      // DeltaS*c / K-scale stages
+  static constexpr int kDsc = kV + ST * DP * 128;    // float [kDS][2][128]
+  static constexpr int kSk = kDsc + kDS * 2 * 512;   // float [kDS][4]
+  static constexpr int kSv = kSk + kDS * 16;         // float [DP]
   static constexpr int kBar = kSv + DP * 4;
-  // q, full[ST], empty[ST], s_full[2], s_free[2], p_full[2][2], pv_done[2][2], drain[2]
-  static constexpr int kNumBars = 1 + 2 * ST + 2 + 2 + 4 + 4 + 2;
+  // q, k_full[ST], k_empty[ST], v_full[ST], v_empty[ST], d_full[kDS], d_empty[kDS], s_full[2],
+  // s_free[2], p_full[2][2], pv_done[2][2], drain[2]
+  static constexpr int kNumBars = 1 + 4 * ST + 2 * kDS + 2 + 2 + 4 + 4 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kBytes = kEnd + 1024;
@@ -801,9 +807,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::kBar);
   uint64_t *q_full = bars;
-  uint64_t *kv_full = bars + 1;
-  uint64_t *kv_empty = kv_full + ST;  // one arrival from each issuer
-  uint64_t *s_full = kv_empty + ST;   // [2] QK_t(j) complete
+  uint64_t *k_full = bars + 1;
+  uint64_t *k_empty = k_full + ST;      // QK_0(n), QK_1(n) complete
+  uint64_t *v_full = k_empty + ST;
+  uint64_t *v_empty = v_full + ST;      // PV_0(n), PV_1(n) complete
+  uint64_t *d_full = v_empty + ST;      // DeltaS*c rows and K scales of tile n
+  uint64_t *d_empty = d_full + P::kDS;  // PV_0(n), PV_1(n) complete
+  uint64_t *s_full = d_empty + P::kDS;  // [2] QK_t(j) complete
   uint64_t *s_free = s_full + 2;      // [2] the softmax of tile t has read S_t(j)
   uint64_t *p_full = s_free + 2;      // [2][2] P~_t(j) written into buffer j % 2, O_t rescaled
   uint64_t *pv_done = p_full + 4;     // [2][2] PV_t(n) complete, by n % 2
@@ -815,8 +825,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kTmaWarp && lane == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < ST; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 2);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < P::kDS; ++i) {
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_empty[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -864,34 +880,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q_full);
       int issued = 0;
       for (int j = 0; j < Tmax; ++j) {
-        const int st = j % ST;
-        if (j >= ST && !mbar_wait_poll<kPollProducerNs>(&kv_empty[st], ((j / ST) - 1) & 1, ab,
+        const int st = j % ST, sd = j % P::kDS;
+        if (j >= ST && !mbar_wait_poll<kPollProducerNs>(&k_empty[st], ((j / ST) - 1) & 1, ab,
                                                          kSiteKvEmpty))
           break;
+        mbar_arrive_expect_tx(&k_full[st], 128 * DP);
+        tma_load_2d(smem + P::kK + st * 128 * DP, &tm_k, 0, yk0 + j * kBKV, &k_full[st]);
+        if (j >= P::kDS && !mbar_wait_poll<kPollProducerNs>(&d_empty[sd], ((j / P::kDS) - 1) & 1,
+                                                              ab, kSiteKvEmpty))
+          break;
         const bool u0 = j < T0, u1 = j < T1;
-        mbar_arrive_expect_tx(&kv_full[st],
-                              128 * DP + DP * 128 + ((u0 ? 1 : 0) + (u1 ? 1 : 0)) * 512 + 16);
-        tma_load_2d(smem + P::kK + st * 128 * DP, &tm_k, 0, yk0 + j * kBKV, &kv_full[st]);
-        tma_load_2d(smem + P::kV + st * DP * 128, &tm_v, s.kvpad0 + j * kBKV, hk * DP,
-                    &kv_full[st]);
-        if (u0) bulk_load(smem + P::kDsc + st * 1024, dsc0 + (size_t)j * kBKV, 512, &kv_full[st]);
+        mbar_arrive_expect_tx(&d_full[sd], ((u0 ? 1 : 0) + (u1 ? 1 : 0)) * 512 + 16);
+        if (u0) bulk_load(smem + P::kDsc + sd * 1024, dsc0 + (size_t)j * kBKV, 512, &d_full[sd]);
         if (u1)
-          bulk_load(smem + P::kDsc + st * 1024 + 512, dsc1 + (size_t)j * kBKV, 512, &kv_full[st]);
-        bulk_load(smem + P::kSk + st * 16, sk_row + j * (kBKV / kGK), 16, &kv_full[st]);
+          bulk_load(smem + P::kDsc + sd * 1024 + 512, dsc1 + (size_t)j * kBKV, 512, &d_full[sd]);
+        bulk_load(smem + P::kSk + sd * 16, sk_row + j * (kBKV / kGK), 16, &d_full[sd]);
         issued = j + 1;
       }
       if (*abort_flag) {  // let the copies already issued land before the CTA exits
         for (int n = issued > ST ? issued - ST : 0; n < issued; ++n)
-          drain_wait(&kv_full[n % ST], (n / ST) & 1);
+          drain_wait(&k_full[n % ST], (n / ST) & 1);
+        for (int n = issued > P::kDS ? issued - P::kDS : 0; n < issued; ++n)
+          drain_wait(&d_full[n % P::kDS], (n / P::kDS) & 1);
         drain_wait(q_full, 0);
       }
+    } else if (warp == 3 && lane == 0) {
+      // ---------------------------------------------------------- V producer (one lane)
+      int issued = 0;
+      for (int j = 0; j < Tmax; ++j) {
+        const int st = j % ST;
+        if (j >= ST && !mbar_wait_poll<kPollProducerNs>(&v_empty[st], ((j / ST) - 1) & 1, ab,
+                                                         kSiteKvEmpty))
+          break;
+        mbar_arrive_expect_tx(&v_full[st], DP * 128);
+        tma_load_2d(smem + P::kV + st * DP * 128, &tm_v, s.kvpad0 + j * kBKV, hk * DP, &v_full[st]);
+        issued = j + 1;
+      }
+      if (*abort_flag)
+        for (int n = issued > ST ? issued - ST : 0; n < issued; ++n)
+          drain_wait(&v_full[n % ST], (n / ST) & 1);
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- Q K^T issuer (one lane)
       // In the fixed order n = 0, 1, ..., tile 0 then tile 1, each with blocking waits: QK_t(n)
       // once the softmax of tile t has read S_t(n-1), PV_t(n-2) is complete (so the softmax
       // knows from s_full_t(n) alone that P~ buffer n % 2 is free, and its own parity waits on
-      // pv_done come at most one phase ahead of what has completed) and K(n) has landed. Stage n
-      // gets this issuer's arrival once QK_0(n) and QK_1(n) complete.
+      // pv_done come at most one phase ahead of what has completed), K(n) and the DeltaS*c of
+      // tile n have landed. K stage n is released once QK_0(n) and QK_1(n) complete.
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128);
       bool ok = mbar_wait(q_full, 0, ab, kSiteQ);
       for (int n = 0; ok && n < Tmax; ++n) {
@@ -902,7 +936,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && n >= 2)
             ok = mbar_wait_poll<kPollQkNs>(&pv_done[2 * t + (n & 1)], ((n - 2) >> 1) & 1, ab,
                                            kSitePvDone);
-          if (ok) ok = mbar_wait(&kv_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
+          if (ok) ok = mbar_wait(&k_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
+          if (ok) ok = mbar_wait(&d_full[n % P::kDS], (n / P::kDS) & 1, ab, kSiteKvFull);
           if (!ok) break;
           tc_fence_after();
           const uint64_t adesc = sdesc_kmajor(smem_u32(smem + P::kQ + t * 128 * DP), DP);
@@ -913,16 +948,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kdesc + (uint64_t)(kk * 2), idesc_qk, kk > 0);
           mma_commit(&s_full[t]);
         }
-        if (ok) mma_commit(&kv_empty[n % ST]);
+        if (ok) mma_commit(&k_empty[n % ST]);
       }
       mma_commit(&drain[0]);  // every MMA issued above completes before tensor memory is freed
       drain_wait(&drain[0], 0);
     } else if (warp == kPvWarp && lane == 0) {
       // ---------------------------------------------------------- P~V issuer (one lane)
-      // Same order: PV_t(n) once P~_t(n) is written (after the rescale of O_t). The kv_full test
-      // is already complete when P~_t(n) exists (QK_t(n) waited for it); it orders the V reads
-      // after the copy for this thread too. Stage n gets this issuer's arrival once PV_0(n) and
-      // PV_1(n) complete.
+      // Same order: PV_t(n) once P~_t(n) is written (after the rescale of O_t) and V(n) has
+      // landed. V stage n and DeltaS*c stage n get this issuer's arrivals once PV_0(n) and PV_1(n)
+      // complete.
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, DP);
       bool ok = true;
       for (int n = 0; ok && n < Tmax; ++n) {
@@ -930,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           if (!ok || n >= (t ? T1 : T0)) continue;
           ok = mbar_wait_poll<kPollPvNs>(&p_full[2 * t + (n & 1)], (n >> 1) & 1, ab, kSitePFull);
-          if (ok) ok = mbar_wait(&kv_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
+          if (ok) ok = mbar_wait(&v_full[n % ST], (n / ST) & 1, ab, kSiteKvFull);
           if (!ok) break;
           tc_fence_after();
           const uint64_t pdesc =
@@ -942,7 +976,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         vdesc + (uint64_t)(kk * 2), idesc_pv, (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&pv_done[2 * t + (n & 1)]);
         }
-        if (ok) mma_commit(&kv_empty[n % ST]);
+        if (ok) {
+          mma_commit(&v_empty[n % ST]);
+          mma_commit(&d_empty[n % P::kDS]);
+        }
       }
       mma_commit(&drain[1]);
       drain_wait(&drain[1], 0);
@@ -989,7 +1026,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool s_ready = false;
 #pragma unroll 1
       for (int j = 0; j < T; ++j) {
-        const int st = j % ST;
         if (!__all_sync(0xffffffffu, s_ready)) {
           ok = warp_all(mbar_wait(&s_full[t], j & 1, ab, kSiteSFull));
           if (!ok) break;
@@ -1006,10 +1042,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[t]);
-        // DeltaS*c and the K scales of stage st: the copy completed kv_full(j), which the Q K^T
+        // DeltaS*c and the K scales of tile j: the copy completed d_full(j), which the Q K^T
         // issuer waited for before issuing QK_t(j), whose completion (s_full) this warp has seen
-        const float *dsc = reinterpret_cast<const float *>(smem + P::kDsc + st * 1024 + t * 512);
-        const float *skv = reinterpret_cast<const float *>(smem + P::kSk + st * 16);
+        const float *dsc =
+            reinterpret_cast<const float *>(smem + P::kDsc + (j % P::kDS) * 1024 + t * 512);
+        const float *skv = reinterpret_cast<const float *>(smem + P::kSk + (j % P::kDS) * 16);
         const int lim = last_key - j * kBKV;
         float2 x[64];
         const float pmax = logits128(x, v, dsc, skv, sqc, lim);

@@ -8,12 +8,13 @@ In both, the agents meet on mbarriers that are waited on by phase parity, as the
 Random interleavings (seeded) are checked for:
   * parity aliasing: a wait must only pass once the awaited phase has completed, and not when
     its barrier has run two phases further;
-  * buffer hazards: S_t, the two P~ buffers of each tile, O_t and the K/V stages are only
-    rewritten once every reader of the old contents is done, and only read once written;
+  * buffer hazards: S_t, the two P~ buffers of each tile, O_t and the K, V and DeltaS stages are
+    only rewritten once every reader of the old contents is done, and only read once written;
   * deadlock: every run finishes.
 The models follow the kernels' conditions one for one. Each has deliberately broken variants
 that must be caught. For the two-tile kernel these are: QK(n) issued without waiting for
-PV(n-2) to complete, and one P~V completion barrier per tile instead of one per P~ buffer. For
+PV(n-2) to complete, one P~V completion barrier per tile instead of one per P~ buffer, and the
+DeltaS stage released with the K stage. For
 the one-tile kernel: the R-free wait removed, and a single-slot alpha ring (a 2-slot ring fails
 as well, while 3 would do; the kernel keeps 4 for mask indexing).
 """
@@ -49,19 +50,24 @@ class Bar:
 
 
 class Model:
-    """attn_pp's protocol. Both issuers take n = 0, 1, ..., tile 0 then tile 1, with blocking
-    waits. QK_t(n) is issued once the softmax read S_t(n-1), PV_t(n-2) completed and K(n) landed;
-    PV_t(n) once P~_t(n) is written; each issuer gives stage n its own arrival (a commit, so once
-    its products reading the stage complete). pv_done[t][b] completes for the PVs of P~ buffer b.
-    The softmax stores P~_t(j), rescales O_t after waiting for PV_t(j-1), then hands P~ over."""
+    """attn_pp's protocol. Three rings: K (ST stages, released by the Q K^T issuer once QK_0(n)
+    and QK_1(n) complete), V (ST stages) and DeltaS*c / K scales (DS stages, read by the softmax),
+    both released by the P~V issuer once PV_0(n) and PV_1(n) complete. One producer loads K and
+    DeltaS, a second one V. Both issuers take n = 0, 1, ..., tile 0 then tile 1, with blocking
+    waits. QK_t(n) is issued once the softmax read S_t(n-1), PV_t(n-2) completed, K(n) and
+    DeltaS(n) landed; PV_t(n) once P~_t(n) is written and V(n) landed. pv_done[t][b] completes
+    for the PVs of P~ buffer b. The softmax stores P~_t(j), rescales O_t after waiting for
+    PV_t(j-1), then hands P~ over."""
 
-    def __init__(self, T0, T1, ST, W, rng, resc_p, qk_after_pv=True, pv_bar_per_buffer=True):
-        self.T, self.ST, self.W, self.rng = (T0, T1), ST, W, rng
+    def __init__(self, T0, T1, ST, W, rng, resc_p, qk_after_pv=True, pv_bar_per_buffer=True,
+                 DS=4, d_released_by_qk=False):
+        self.T, self.ST, self.DS, self.W, self.rng = (T0, T1), ST, DS, W, rng
         self.Tmax = max(T0, T1)
-        self.resc_p, self.qk_after_pv = resc_p, qk_after_pv
+        self.resc_p, self.qk_after_pv, self.d_released_by_qk = resc_p, qk_after_pv, \
+            d_released_by_qk
         B = Bar
-        self.kv_full = [B(f"kv_full{s}", 1) for s in range(ST)]
-        self.kv_empty = [B(f"kv_empty{s}", 2) for s in range(ST)]
+        self.full = {r: [B(f"{r}_full{s}", 1) for s in range(self.depth(r))] for r in "kvd"}
+        self.empty = {r: [B(f"{r}_empty{s}", 1) for s in range(self.depth(r))] for r in "kvd"}
         self.s_full = [B(f"s_full{t}", 1) for t in range(2)]
         self.s_free = [B(f"s_free{t}", W) for t in range(2)]
         self.p_full = [[B(f"p_full{t}{b}", W) for b in range(2)] for t in range(2)]
@@ -73,8 +79,8 @@ class Model:
             self.pv_done = [[one[t], one[t]] for t in range(2)]
             self.pv_phase = lambda n: n
         self.pipes = {"qk": [], "pv": []}   # one in-order pipe per issuing thread
-        self.stage = [None] * ST             # KV tile held by each stage
-        self.stage_users = {}                # tile -> readers not yet done
+        self.stage = {r: [None] * self.depth(r) for r in "kvd"}  # tile held by each stage
+        self.stage_users = {r: {} for r in "kvd"}                # tile -> readers not yet done
         self.S = [None, None]                # QK index whose result S_t holds
         self.s_read = [[-1] * W for _ in range(2)]   # last S_t(j) read by each warp
         self.P = [[[None] * W for _ in range(2)] for _ in range(2)]  # P~ tile in buffer
@@ -82,35 +88,44 @@ class Model:
         self.events = 0                      # steps taken by agents other than the issuers
 
     # ------------------------------------------------------------ helpers
-    def use_stage(self, n, who):
-        s = n % self.ST
-        if self.stage[s] != n:
-            raise Hazard(f"{who} reads KV tile {n} but stage {s} holds {self.stage[s]}")
+    def depth(self, ring):
+        return self.DS if ring == "d" else self.ST
 
-    def release_stage_user(self, n, who):
-        self.stage_users[n].discard(who)
+    def use_stage(self, ring, n, who):
+        s = n % self.depth(ring)
+        if self.stage[ring][s] != n:
+            raise Hazard(f"{who} reads {ring} tile {n} but stage {s} holds {self.stage[ring][s]}")
+
+    def release_stage_user(self, ring, n, who):
+        self.stage_users[ring][n].discard(who)
 
     def pv_wait(self, t, n):
         """The barrier and phase that PV_t(n)'s completion moves."""
         return self.pv_done[t][n & 1], self.pv_phase(n)
 
     # ------------------------------------------------------------ agents (generators)
-    def producer(self):
+    def load(self, ring, j, users):
+        d = self.depth(ring)
+        s = j % d
+        if j >= d:
+            yield ("wait", self.empty[ring][s], j // d - 1)
+            old = j - d
+            if self.stage_users[ring].get(old):
+                raise Hazard(f"{ring} stage {s} reloaded while "
+                             f"{sorted(self.stage_users[ring][old])} still read tile {old}")
+        self.stage[ring][s] = j
+        self.stage_users[ring][j] = users
+        yield ("act", self.full[ring][s].arrive)
+
+    def producer(self):  # K and DeltaS
         for j in range(self.Tmax):
-            s = j % self.ST
-            if j >= self.ST:
-                yield ("wait", self.kv_empty[s], j // self.ST - 1)
-                old = j - self.ST
-                if self.stage_users.get(old):
-                    raise Hazard(f"stage {s} reloaded while {sorted(self.stage_users[old])} "
-                                 f"still read KV tile {old}")
-            self.stage[s] = j
-            users = set()
-            for t in range(2):
-                if j < self.T[t]:
-                    users |= {("QK", t), ("PV", t)} | {("SM", t, w) for w in range(self.W)}
-            self.stage_users[j] = users
-            yield ("act", self.kv_full[s].arrive)
+            live = [t for t in range(2) if j < self.T[t]]
+            yield from self.load("k", j, {("QK", t) for t in live})
+            yield from self.load("d", j, {("SM", t, w) for t in live for w in range(self.W)})
+
+    def producer_v(self):
+        for j in range(self.Tmax):
+            yield from self.load("v", j, {("PV", t) for t in range(2) if j < self.T[t]})
 
     def qk_issuer(self):
         """Fixed order n = 0, 1, ..., tile 0 then tile 1, each condition a blocking wait."""
@@ -122,11 +137,14 @@ class Model:
                     yield ("wait", self.s_free[t], n - 1)
                 if self.qk_after_pv and n >= 2:
                     yield ("wait", *self.pv_wait(t, n - 2))
-                yield ("wait", self.kv_full[n % self.ST], n // self.ST)
+                yield ("wait", self.full["k"][n % self.ST], n // self.ST)
+                yield ("wait", self.full["d"][n % self.DS], n // self.DS)
                 if n > 0 and min(self.s_read[t]) < n - 1:
                     raise Hazard(f"QK{t}({n}) issued before S{t}({n - 1}) was read")
                 self.pipes["qk"] += [("QK", t, n), ("commit", self.s_full[t])]
-            self.pipes["qk"].append(("commit", self.kv_empty[n % self.ST]))
+            self.pipes["qk"].append(("commit", self.empty["k"][n % self.ST]))
+            if self.d_released_by_qk:
+                self.pipes["qk"].append(("commit", self.empty["d"][n % self.DS]))
 
     def pv_issuer(self):
         for n in range(self.Tmax):
@@ -134,14 +152,16 @@ class Model:
                 if n >= self.T[t]:
                     continue
                 yield ("wait", self.p_full[t][n & 1], n >> 1)
-                yield ("wait", self.kv_full[n % self.ST], n // self.ST)
+                yield ("wait", self.full["v"][n % self.ST], n // self.ST)
                 for w in range(self.W):
                     if self.P[t][n & 1][w] != n:
                         raise Hazard(f"PV{t}({n}) issued but warp {w}'s P~ buffer holds "
                                      f"{self.P[t][n & 1][w]}")
                 bar, _ = self.pv_wait(t, n)
                 self.pipes["pv"] += [("PV", t, n), ("commit", bar)]
-            self.pipes["pv"].append(("commit", self.kv_empty[n % self.ST]))
+            self.pipes["pv"].append(("commit", self.empty["v"][n % self.ST]))
+            if not self.d_released_by_qk:
+                self.pipes["pv"].append(("commit", self.empty["d"][n % self.DS]))
 
     def pipe_step(self, name):
         kind = self.pipes[name].pop(0)
@@ -150,15 +170,15 @@ class Model:
             return
         _, t, n = kind
         if kind[0] == "QK":
-            self.use_stage(n, f"QK{t}({n})")
+            self.use_stage("k", n, f"QK{t}({n})")
             self.S[t] = n
-            self.release_stage_user(n, ("QK", t))
+            self.release_stage_user("k", n, ("QK", t))
         else:
-            self.use_stage(n, f"PV{t}({n})")
+            self.use_stage("v", n, f"PV{t}({n})")
             if self.pv_completed[t] != n:
                 raise Hazard(f"PV{t}({n}) out of order")
             self.pv_completed[t] += 1
-            self.release_stage_user(n, ("PV", t))
+            self.release_stage_user("v", n, ("PV", t))
 
     def softmax(self, t, w):
         T = self.T[t]
@@ -168,8 +188,9 @@ class Model:
                 raise Hazard(f"softmax{t}.{w} reads S{t}({j}) but S holds {self.S[t]}")
             self.s_read[t][w] = j
             yield ("act", self.s_free[t].arrive)
-            self.use_stage(j, f"softmax{t}.{w} DeltaS({j})")  # landed: QK_t(j) waited for it
-            self.release_stage_user(j, ("SM", t, w))
+            yield ("act", lambda: None)  # the logits read DeltaS(j) (landed: QK_t(j) waited)
+            self.use_stage("d", j, f"softmax{t}.{w} DeltaS({j})")
+            self.release_stage_user("d", j, ("SM", t, w))
             # P~_t(j) is stored while the exponentials run, before the rescale
             if self.pv_completed[t] < j - 1:
                 raise Hazard(f"softmax{t}.{w} overwrites P~ buffer {j & 1} before PV{t}({j - 2})")
@@ -190,7 +211,8 @@ class Model:
 
     # ------------------------------------------------------------ scheduler
     def run(self, max_steps=300000):
-        agents = {"producer": self.producer(), "qk": self.qk_issuer(), "pv": self.pv_issuer()}
+        agents = {"producer": self.producer(), "producer_v": self.producer_v(),
+                  "qk": self.qk_issuer(), "pv": self.pv_issuer()}
         for t in range(2):
             for w in range(self.W):
                 agents[f"sm{t}{w}"] = self.softmax(t, w)
@@ -246,15 +268,16 @@ class Model:
         raise Hazard("step limit")
 
 
-CASES = [(T0, T1, ST) for (T0, T1) in [(0, 1), (1, 1), (1, 2), (2, 3), (3, 3), (5, 6), (4, 4),
-                                       (0, 3), (6, 2), (9, 10)] for ST in (2, 3, 6)]
+CASES = [(T0, T1, ST, DS) for (T0, T1) in [(0, 1), (1, 1), (1, 2), (2, 3), (3, 3), (5, 6), (4, 4),
+                                           (0, 3), (6, 2), (9, 10)]
+         for ST, DS in ((2, 2), (3, 4), (6, 4), (3, 6))]
 
 
-@pytest.mark.parametrize("T0,T1,ST", CASES)
-def test_two_tile_protocol_has_no_aliasing_hazard_or_deadlock(T0, T1, ST):
+@pytest.mark.parametrize("T0,T1,ST,DS", CASES)
+def test_two_tile_protocol_has_no_aliasing_hazard_or_deadlock(T0, T1, ST, DS):
     for seed in range(40):
-        rng = random.Random(seed * 1009 + T0 * 31 + T1 * 7 + ST)
-        Model(T0, T1, ST, W=2, rng=rng, resc_p=rng.choice([0.0, 0.15, 0.5, 1.0])).run()
+        rng = random.Random(seed * 1009 + T0 * 31 + T1 * 7 + ST + 13 * DS)
+        Model(T0, T1, ST, W=2, rng=rng, resc_p=rng.choice([0.0, 0.15, 0.5, 1.0]), DS=DS).run()
 
 
 def _caught(**kw):
@@ -272,6 +295,12 @@ def test_model_catches_qk_issued_before_pv_two_back_completed():
     """QK(n) before PV(n-2) completes lets the softmax refill the P~ buffer that PV(n-2) has not
     read yet."""
     assert _caught(qk_after_pv=False)
+
+
+def test_model_catches_deltas_stage_released_after_the_qk_products():
+    """Releasing a DeltaS*c stage when the Q K^T products complete lets the producer refill it
+    while the softmax still reads it."""
+    assert _caught(d_released_by_qk=True)
 
 
 def test_model_catches_one_pv_barrier_per_tile():
