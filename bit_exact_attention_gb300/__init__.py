@@ -22,9 +22,9 @@ from ._lib import BF16, FP16, FP32, Sage2Error, WsLayout  # noqa: F401
 __all__ = ["attn_fwd", "attn_fwd_varlen", "prepass", "attention", "prepass_varlen",
            "attention_varlen", "workspace_size", "workspace_layout", "device_status",
            "alloc_workspace", "debug_tile", "debug_timeout", "Sage2Error", "load_library",
-           "attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "quant_flags", "QUANT_NO_SMOOTH_Q",
-           "QUANT_NO_SMOOTH_K", "QUANT_PER_BLOCK", "QUANT_SAGE1", "attn_fwd_host",
-           "host_scratch_size", "host_status"]
+           "attn_fwd_noalloc", "noalloc_status", "NOALLOC_SCRATCH_BYTES", "quant_flags",
+           "QUANT_NO_SMOOTH_Q", "QUANT_NO_SMOOTH_K", "QUANT_PER_BLOCK", "QUANT_SAGE1",
+           "attn_fwd_host", "host_scratch_size", "host_status"]
 
 _DT = {torch.float16: FP16, torch.bfloat16: BF16, torch.float32: FP32}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # SAGE2_NOALLOC_SCRATCH_BYTES in include/sage2_attn.h
@@ -323,3 +323,10 @@ def attn_fwd_noalloc(q, k, v, out, causal=False, sm_scale=0.0, stream=None):
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _code(q.dtype), _code(out.dtype), B, Hq, Hkv, Nq,
         Nkv, D, int(bool(causal)), float(sm_scale), _stream(stream)), "sage2_attn_fwd_noalloc")
     return out
+
+
+def noalloc_status(stream=None) -> tuple[int, int]:
+    """(status code, raw word) of the last attn_fwd_noalloc call on the current device."""
+    raw = ctypes.c_int(0)
+    rc = _lib.lib().sage2_noalloc_status(_stream(stream), ctypes.byref(raw))
+    return int(rc), int(raw.value)

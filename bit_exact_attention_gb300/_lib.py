@@ -59,6 +59,7 @@ def _declare(lib):
         "sage2_attention_varlen": ([P, i, P, P, i, i, i, i, i, i, i, i, i, f, P, sz, P], i),
         "sage2_attention_varlen_ex": ([P, i, P, P, i, i, i, i, i, i, i, i, i, f, i, P, sz, P], i),
         "sage2_device_status": ([P, P, ctypes.POINTER(i)], i),
+        "sage2_noalloc_status": ([P, ctypes.POINTER(i)], i),
         "sage2_debug_tile": ([P, P, i, i, i, i, i, i, i, i, i, f, P, sz, i, i, i, i, P, P, P, P], i),
         "sage2_debug_tile_ex": ([P, P, i, i, i, i, i, i, i, i, i, f, i, P, sz, i, i, i, i, P, P, P, P],
                                 i),

@@ -67,3 +67,10 @@ extern "C" int sage2_attn_fwd_noalloc(const void *q, const void *k, const void *
   return sage2_attn_fwd(q, k, v, out, in_dtype, out_dtype, B, Hq, Hkv, Nq, Nkv, D, causal,
                         sm_scale, scratch, kScratchBytes, stream);
 }
+
+extern "C" int sage2_noalloc_status(void *stream, int *raw) {
+  void *scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != SAGE2_OK) return rc;
+  return sage2_device_status(scratch, stream, raw);
+}

@@ -263,6 +263,14 @@ int sage2_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *ou
                            int out_dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                            int causal, float sm_scale, void *stream);
 
+/* Device status of the noalloc scratch on the current device, the sage2_device_status of the
+ * workspace that sage2_attn_fwd_noalloc uses: synchronizes `stream`, then reads the status word
+ * of the last noalloc call. Returns SAGE2_OK, SAGE2_EINVAL (a sequence exceeded its bound, or
+ * the code format was wrong) or SAGE2_EDEVICE_TIMEOUT (a device-side wait gave up; the wait
+ * site is in the low byte of *raw); SAGE2_ECUDA if the scratch or the word cannot be read.
+ * `raw` (may be NULL) receives the status word. */
+int sage2_noalloc_status(void *stream, int *raw);
+
 #ifdef __cplusplus
 }
 #endif
