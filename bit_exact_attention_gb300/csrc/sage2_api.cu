@@ -37,7 +37,7 @@ bool make_layout(int B, int Hq, int Hkv, int max_nq, int max_nkv, int Dp, int to
     return o;
   };
   L->code_bytes = code_bytes;
-  L->status = take(256);
+  L->status = take(4 * (kSeqOrderWord + (size_t)B));
   L->qcode = take((size_t)Hq * tq * Dp * code_bytes);
   L->kcode = take((size_t)Hkv * tkv * Dp * code_bytes);
   L->vcodeT = take((size_t)Hkv * Dp * tkv);

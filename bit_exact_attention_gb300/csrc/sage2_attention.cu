@@ -101,6 +101,7 @@ struct AttnArgs {
   void *out;
   int out_dtype;
   int *status;
+  const int *seq_order;  // varlen: the sequence each z index takes (two-tile kernel)
   AttnDebug dbg;
 };
 
@@ -812,9 +813,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Geometry &g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int format = a.status[1];
-  const int b = DBG ? a.dbg.b : (int)blockIdx.z, hq = DBG ? a.dbg.h : (int)blockIdx.y;
-  const int pair = DBG ? a.dbg.qt / 2
-                       : (g.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
+  // Launch order (the order CTAs start in): z sequences, longest K/V first for varlen calls
+  // (the prepass's order); within a sequence the pairs in x-major (pair index, q head) order,
+  // heaviest pair first under causal masks, all heads of a pair index together. Starting the
+  // longest CTAs first keeps them out of the tail.
+  int b = (int)blockIdx.z;
+  if (!DBG && g.cu_kv) {
+    const int ob = a.seq_order[blockIdx.z];
+    if (ob >= 0 && ob < g.B) b = ob;  // (a workspace of another prepass keeps the batch order)
+  }
+  if (DBG) b = a.dbg.b;
+  const int npairs = (int)gridDim.x / g.Hq, pidx = (int)blockIdx.x / g.Hq;
+  const int hq = DBG ? a.dbg.h : (int)blockIdx.x % g.Hq;
+  const int pair = DBG ? a.dbg.qt / 2 : (g.causal ? npairs - 1 - pidx : pidx);
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
   if (format != kFormatInt4) {
     if (tid == 0) atomicCAS(a.status, 0, kStatusFormat);
@@ -1276,6 +1287,7 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
   a.out = out;
   a.out_dtype = out_dtype;
   a.status = w.status;
+  a.seq_order = w.status + kSeqOrderWord;
   a.dbg = dbg ? *dbg : AttnDebug{0, 0, 0, 0, nullptr, nullptr, nullptr, 0};
   const CUtensorMapSwizzle qk_sw =
       g.Dp == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -1292,7 +1304,7 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
     CUtensorMap mq;
     if (!make_map(&mq, w.qcode, g.Dp, (uint64_t)g.Hq * L.Tq, g.Dp, 128, qk_sw))
       return cudaErrorInvalidValue;
-    const dim3 grid2((nqt + 1) / 2, g.Hq, g.B);
+    const dim3 grid2(g.Hq * ((nqt + 1) / 2), 1, g.B);
     // K and V stages: 3 each at D = 128; 8 each at D = 64 (no P~ buffers in shared memory there;
     // 8 measured 1.5 % faster than 6 on the video DiT shape, 10 no better)
     if (dbg) {

@@ -38,6 +38,14 @@ struct Layout {
 bool make_layout(int B, int Hq, int Hkv, int max_nq, int max_nkv, int Dp, int total_q,
                  int total_kv, int code_bytes, Layout *L);
 
+// The workspace status area: word 0 the device status, word 1 the code format, words
+// kSeqOrderWord .. + B - 1 the order in which the two-tile attention kernel takes the sequences
+// of a varlen call (longest K/V first; written by the prepass).
+constexpr int kSeqOrderWord = 64;
+// The prepass sorts at most this many sequences (a rank count per sequence in one CTA); larger
+// batches keep their own order.
+constexpr int kSeqOrderMaxSort = 256;
+
 // Code format a prepass leaves in word 1 of the workspace status area (every byte of the word
 // the same), checked by the attention kernel before it reads anything else.
 constexpr unsigned char kFormatInt4Byte = 0x34, kFormatInt8Byte = 0x38;

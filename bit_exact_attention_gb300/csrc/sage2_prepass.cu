@@ -825,6 +825,25 @@ __global__ void __launch_bounds__(kDsThreads, 1) delta_s_tc(PrepassArgs a) {
   if (warp == kDsMmaWarp) tmem_dealloc(tbase, 512);
 }
 
+// The order in which the two-tile attention kernel takes the sequences of a varlen call: by
+// decreasing K/V length (the length of every CTA's loop), ties by index, so that the longest
+// CTAs start first and the short ones fill the tail. One CTA; a rank count per sequence, for at
+// most kSeqOrderMaxSort sequences (beyond that the batch keeps its order).
+__global__ void __launch_bounds__(256) seq_order(const int *cu_kv, int B, int *order) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    int rank = b;
+    if (B <= kSeqOrderMaxSort) {
+      const int n = cu_kv[b + 1] - cu_kv[b];
+      rank = 0;
+      for (int c = 0; c < B; ++c) {
+        const int m = cu_kv[c + 1] - cu_kv[c];
+        rank += (m > n || (m == n && c < b)) ? 1 : 0;
+      }
+    }
+    order[rank] = b;  // ranks are a permutation of 0 .. B - 1 (a strict total order)
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
@@ -845,6 +864,7 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   // the code format, checked by the attention kernel
   e = cudaMemsetAsync(a.w.status + 1, int8 ? kFormatInt8Byte : kFormatInt4Byte, sizeof(int), st);
   if (e != cudaSuccess) return e;
+  if (g.cu_kv) seq_order<<<1, 256, 0, st>>>(g.cu_kv, g.B, a.w.status + kSeqOrderWord);
 
   const int nvec = g.Hkv * g.D0 / 8;
   // every grid dimension at least 1 (a zero-length maximum is legal; the kernels bound-check)

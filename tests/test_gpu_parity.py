@@ -67,6 +67,20 @@ def run_case(name):
 
 
 # ------------------------------------------------------------------ prepass
+def test_prepass_orders_varlen_sequences_longest_kv_first():
+    """The prepass leaves, after the status and format words, the order in which the two-tile
+    kernel takes the sequences of a varlen call: a permutation by decreasing K/V length, ties by
+    index (the kernel then starts its longest CTAs first)."""
+    w = W.scaled(W.VARLEN, (300, 77, 129, 5, 0), (500, 129, 1000, 129, 64), name="order_s")
+    x = W.make_inputs(w)
+    g = GpuCase(w, x)
+    g.prepass()
+    torch.cuda.synchronize()
+    order = g._buf(g.L.status + 4 * 64, w.batch, torch.int32).cpu().numpy().tolist()
+    want = sorted(range(w.batch), key=lambda b: (-w.nkv[b], b))
+    assert order == want, (order, want)
+
+
 @pytest.mark.parametrize("name", list(SCALED))
 def test_prepass_codes_bit_exact_delta_s_bounded(name):
     w, x, g = run_case(name)
