@@ -303,9 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     hq = a.dbg.h;
     qt = a.dbg.qt;
   } else {
+    // launch order as in attn_pp: varlen sequences longest K/V first, then (tile x head) with
+    // all heads of a tile index together, heaviest first under causal masks
     b = blockIdx.z;
-    hq = blockIdx.y;
-    qt = g.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    if (g.cu_kv) {
+      const int ob = a.seq_order[blockIdx.z];
+      if (ob >= 0 && ob < g.B) b = ob;
+    }
+    hq = (int)blockIdx.x % g.Hq;
+    const int ntiles = (int)gridDim.x / g.Hq, tidx = (int)blockIdx.x / g.Hq;
+    qt = g.causal ? ntiles - 1 - tidx : tidx;
   }
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
   if (format != (I8 ? kFormatInt8 : kFormatInt4)) {  // a workspace of the other code format
@@ -1314,7 +1321,7 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
     if (g.Dp == 128) return launch_pp<128, 3, false>(mq, mk, mv, a, grid2, st);
     return launch_pp<64, 8, false>(mq, mk, mv, a, grid2, st);
   }
-  const dim3 grid = dbg ? dim3(1) : dim3(nqt, g.Hq, g.B);
+  const dim3 grid = dbg ? dim3(1) : dim3(g.Hq * nqt, 1, g.B);
   // pipeline depth: as many K/V stages as fit (a stage of fp16 K codes is twice as large)
   if (int8_qk) {
     if (dbg) {
