@@ -352,6 +352,21 @@ def per_config_figures(S, names, dev, flush, stream, qf, peak, hbm_gbs, steps=5,
                        "prepass_gbs": round(gbs, 1),
                        "prepass_frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None,
                        "metric_ops": ops, "steps": steps}
+        if len(w.nq) > 1 and len(set(zip(w.nq, w.nkv))) > 1:
+            # each sequence of a mixed batch alone: its kernel-only figures (a short-Nq, long-Nkv
+            # sequence has few Q tiles, so few CTAs: the whole batch is what fills the GPU)
+            seqs = []
+            for b, (nq, nkv) in enumerate(zip(w.nq, w.nkv)):
+                wb = W.scaled(w, (nq,), (nkv,), name=f"{w.name}_seq{b}")
+                _, att_b = time_workload(S, wb, dev, steps, warmup, flush, stream, qf)
+                a_b = statistics.median(att_b)
+                kern_b = wb.metric_ops() / (a_b / 1e3) / 1e12
+                tiles = -(-nq // 128)  # one CTA per Q tile (v1 path) or per pair of Q tiles
+                ctas = (tiles if qf & S.QUANT_SAGE1 else (tiles + 1) // 2) * w.hq
+                seqs.append({"nq": nq, "nkv": nkv, "attention_ms": round(a_b, 4),
+                             "kernel_only_tops": round(kern_b, 2),
+                             "roofline_frac": round(kern_b / peak, 4), "ctas": ctas})
+            res[w.name]["sequences_alone"] = seqs
     return res
 
 
