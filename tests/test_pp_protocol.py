@@ -60,11 +60,12 @@ class Model:
     PV_t(j-1), then hands P~ over."""
 
     def __init__(self, T0, T1, ST, W, rng, resc_p, qk_after_pv=True, pv_bar_per_buffer=True,
-                 DS=4, d_released_by_qk=False):
+                 DS=4, d_released_by_qk=False, sm_weight=1.0):
         self.T, self.ST, self.DS, self.W, self.rng = (T0, T1), ST, DS, W, rng
         self.Tmax = max(T0, T1)
         self.resc_p, self.qk_after_pv, self.d_released_by_qk = resc_p, qk_after_pv, \
             d_released_by_qk
+        self.sm_weight = sm_weight  # < 1: softmax warps take steps less often (slow softmax)
         B = Bar
         self.full = {r: [B(f"{r}_full{s}", 1) for s in range(self.depth(r))] for r in "kvd"}
         self.empty = {r: [B(f"{r}_empty{s}", 1) for s in range(self.depth(r))] for r in "kvd"}
@@ -238,6 +239,10 @@ class Model:
                 raise Hazard("deadlock: " + ", ".join(
                     f"{k}:{pending[k][0]} {getattr(pending[k][1], 'name', '')}"
                     for k in agents if pending[k]))
+            if self.sm_weight < 1.0:
+                fast = [k for k in runnable if not (isinstance(k, str) and k.startswith("sm"))
+                        or self.rng.random() < self.sm_weight]
+                runnable = fast or runnable
             k = self.rng.choice(runnable)
             if k not in ("qk", "pv"):
                 self.events += 1
@@ -277,7 +282,8 @@ CASES = [(T0, T1, ST, DS) for (T0, T1) in [(0, 1), (1, 1), (1, 2), (2, 3), (3, 3
 def test_two_tile_protocol_has_no_aliasing_hazard_or_deadlock(T0, T1, ST, DS):
     for seed in range(40):
         rng = random.Random(seed * 1009 + T0 * 31 + T1 * 7 + ST + 13 * DS)
-        Model(T0, T1, ST, W=2, rng=rng, resc_p=rng.choice([0.0, 0.15, 0.5, 1.0]), DS=DS).run()
+        Model(T0, T1, ST, W=2, rng=rng, resc_p=rng.choice([0.0, 0.15, 0.5, 1.0]), DS=DS,
+              sm_weight=rng.choice([1.0, 0.1])).run()
 
 
 def _caught(**kw):
@@ -285,7 +291,8 @@ def _caught(**kw):
         rng = random.Random(seed)
         T0, T1 = rng.choice([(3, 4), (4, 4), (5, 6), (2, 3)])
         try:
-            Model(T0, T1, 3, W=2, rng=rng, resc_p=rng.choice([0.0, 0.5]), **kw).run()
+            Model(T0, T1, 3, W=2, rng=rng, resc_p=rng.choice([0.0, 0.5]),
+                  sm_weight=rng.choice([1.0, 0.1]), **kw).run()
         except Hazard:
             return True
     return False
