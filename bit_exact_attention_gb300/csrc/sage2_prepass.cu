@@ -180,25 +180,31 @@ __global__ void __launch_bounds__(kStatThreads) kv_stats_partial(PrepassArgs a) 
   }
 }
 
-// grid (B * Hkv, Dp / 32), block 1024 = 32 channels x 32 parts: part p sums chunks p, p + 32,
-// ... in FP64, then the parts are added in order. The chunk sums are exact (see above), and so
-// is every FP64 sum of them for 16-bit inputs, so the order does not change the result.
-constexpr int kFinalThreads = 1024, kFinalChan = 32, kFinalParts = kFinalThreads / kFinalChan;
+// grid (B * Hkv, Dp / CH), block 1024 = CH channels x 1024 / CH parts: part p sums chunks p,
+// p + parts, ... in FP64, then the parts are added pairwise in a fixed tree. The chunk sums are
+// exact (see above), and so is every FP64 sum of them for 16-bit inputs, so the order does not
+// change the result. CH = 32 when the grid already has enough blocks; CH = 8 (128 parts, so
+// each thread adds few chunks) when it has few, as for a single kv head, where this reduction
+// is otherwise a chain of dependent loads on a handful of SMs.
+constexpr int kFinalThreads = 1024;
+template <int CH>
 __global__ void __launch_bounds__(kFinalThreads) kv_stats_final(PrepassArgs a) {
-  __shared__ double psum[kFinalParts][kFinalChan];
-  __shared__ float pmax[kFinalParts][kFinalChan];
+  constexpr int kParts = kFinalThreads / CH;
+  __shared__ double psum[kParts][CH];
+  __shared__ float pmax[kParts][CH];
   const Geometry &g = a.g;
   const int b = blockIdx.x / g.Hkv, h = blockIdx.x % g.Hkv;
-  const int dl = threadIdx.x % kFinalChan, part = threadIdx.x / kFinalChan;
-  const int d = blockIdx.y * kFinalChan + dl;
+  const int dl = threadIdx.x % CH, part = threadIdx.x / CH;
+  const int d = blockIdx.y * CH + dl;
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
+  const bool live = s.ok && d < g.D0 && s.nkv > 0;
   double sum = 0.0;
   float amax = 0.f;
-  if (s.ok && d < g.D0 && s.nkv > 0) {
+  if (live) {
     const int nch = (s.nkv + kStatChunk - 1) / kStatChunk;
     const int row_elems = g.Hkv * g.D0;
 #pragma unroll 4
-    for (int c = part; c < nch; c += kFinalParts) {
+    for (int c = part; c < nch; c += kParts) {
       const size_t po = ((size_t)b * a.L.nchunk + c) * row_elems + (size_t)h * g.D0 + d;
       sum += a.w.kpart[po];
       amax = fmaxf(amax, a.w.vpart[po]);
@@ -207,15 +213,20 @@ __global__ void __launch_bounds__(kFinalThreads) kv_stats_final(PrepassArgs a) {
   psum[part][dl] = sum;
   pmax[part][dl] = amax;
   __syncthreads();
-  if (part != 0) return;
-  for (int p = 1; p < kFinalParts; ++p) {
-    sum += psum[p][dl];
-    amax = fmaxf(amax, pmax[p][dl]);
+#pragma unroll
+  for (int n = kParts / 2; n >= 1; n >>= 1) {
+    if (part < n) {
+      psum[part][dl] += psum[part + n][dl];
+      pmax[part][dl] = fmaxf(pmax[part][dl], pmax[part + n][dl]);
+    }
+    __syncthreads();
   }
+  if (part != 0) return;
+  sum = psum[0][dl];
+  amax = pmax[0][dl];
   const size_t o = ((size_t)b * g.Hkv + h) * g.Dp + d;
   float mean = 0.f;
-  if (s.ok && d < g.D0 && s.nkv > 0)
-    mean = (a.flags & SAGE2_QUANT_NO_SMOOTH_K) ? 0.f : (float)(sum / (double)s.nkv);
+  if (live) mean = (a.flags & SAGE2_QUANT_NO_SMOOTH_K) ? 0.f : (float)(sum / (double)s.nkv);
   a.w.kmean[o] = mean;
   a.w.vscale[o] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
   a.w.vinv[o] = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
@@ -886,7 +897,10 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
     constexpr bool BF = decltype(bf_tag)::value;
     constexpr bool I8 = decltype(i8_tag)::value;
     kv_stats_partial<BF><<<stat_grid, kStatThreads, 0, st>>>(a);
-    kv_stats_final<<<dim3(g.B * g.Hkv, g.Dp / kFinalChan), kFinalThreads, 0, st>>>(a);
+    if (g.B * g.Hkv * (g.Dp / 32) >= 64)
+      kv_stats_final<32><<<dim3(g.B * g.Hkv, g.Dp / 32), kFinalThreads, 0, st>>>(a);
+    else
+      kv_stats_final<8><<<dim3(g.B * g.Hkv, g.Dp / 8), kFinalThreads, 0, st>>>(a);
     k_quant<DP, BF, I8><<<kv_grid, 256, 0, st>>>(a);
     v_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
     q_quant<DP, BF, I8><<<q_grid, 256, 0, st>>>(a);
