@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -36,7 +37,8 @@ namespace {
 
 struct PrepassArgs {
   const uint16_t *q, *k, *v;
-  int flags;  // sage2_quant_flags
+  int flags;     // sage2_quant_flags
+  int ds_chunk;  // delta_s_tc: key tiles per CTA
   Geometry g;
   Layout L;
   WsPtrs w;
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
 // ones are below 2^-23 of |qmean_d K~_jd|, and the accumulator rounds once per MMA step
 // (6 x D / 16 steps), so the result lies within about 50 units of 2^-24 of
 // sum_d |qmean_d K~_jd| of the exact dot product.
-// One CTA per (128-row tile, chunk of kDsChunk key tiles, sequence x kv head); warps:
+// One CTA per (128-row tile, chunk of ds_chunk key tiles, sequence x kv head); warps:
 //   0-7  per key tile K~ of 32 keys x half the channels per warp: each load instruction reads
 //        whole 128-byte row segments (DP / 16 lanes per segment), and each lane splits its
 //        8 channels and stores the three 16-byte pieces straight into their swizzled places in
@@ -552,7 +554,11 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
 //        for the key tiles each row's Q block visits;
 //   12   MMA issuer (one lane); it also allocates tensor memory.
 // Tensor memory: the qmean pieces at [0, 3 DP / 2), two 128-column accumulators at 256 and 384.
-constexpr int kDsChunk = 16;  // key tiles per CTA
+// key tiles per CTA: 16, 8 or 4, whichever gives the least waves x (key tiles per CTA + the
+// per-CTA set-up, measured at about 3 key tiles' time; ties to the larger chunk). With few heads
+// a grid of 16-tile CTAs can cover under half the SMs (causal rows see few key tiles), and a
+// smaller chunk fills them; with many, the set-up of more CTAs outweighs the shorter tail.
+constexpr int kDsChunkMax = 16, kDsChunkMin = 4, kDsCtaSetupTiles = 3;
 constexpr int kDsThreads = 416, kDsLoadWarps = 8, kDsMmaWarp = 12;  // epilogue: warps 8-11
 
 template <int DP>
@@ -609,7 +615,7 @@ __global__ void __launch_bounds__(kDsThreads, 1) delta_s_tc(PrepassArgs a) {
   const int ntile_kv = (s.nkv + kBKV - 1) / kBKV;
   const int qb_last = min(nrows - 1, r0 + 127) / grp;
   const int t_end_all = g.causal ? kv_tiles_for(qb_last, s.nq, s.nkv, 1) : ntile_kv;
-  const int t0 = blockIdx.x * kDsChunk, t1 = min(t_end_all, t0 + kDsChunk);
+  const int t0 = blockIdx.x * a.ds_chunk, t1 = min(t_end_all, t0 + a.ds_chunk);
   if (t0 >= t1) return;
   const int nt = t1 - t0;
 
@@ -885,9 +891,38 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   const dim3 stat_grid(L.nchunk, g.B, (nvec + stat_vpb - 1) / stat_vpb);
   const dim3 kv_grid(kv_tiles, g.Hkv, g.B);
   const dim3 q_grid(q_tiles, g.Hq, g.B);
-  // DeltaS: 128-row tiles of (Q block, q head) pairs, kDsChunk key tiles per CTA
+  // DeltaS: 128-row tiles of (Q block, q head) pairs, a.ds_chunk key tiles per CTA
   const int max_rows = (g.Hq / g.Hkv) * q_tiles;
-  const dim3 ds_grid((kv_tiles + kDsChunk - 1) / kDsChunk, (max_rows + 127) / 128, g.B * g.Hkv);
+  const int row_tiles = (max_rows + 127) / 128;
+  int nsm = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    nsm = 0;
+  a.ds_chunk = kDsChunkMax;
+  if (nsm > 0) {
+    // CTAs with work per chunk size: a dense call's row tile rt visits the key tiles of its last
+    // Q block (all of them without a causal mask); a varlen call's lengths live on the device,
+    // so every chunk of the longest sequence counts
+    long long best = -1;
+    for (int ch = kDsChunkMax; ch >= kDsChunkMin; ch /= 2) {
+      long long active = 0;
+      for (int rt = 0; rt < row_tiles; ++rt) {
+        int t_end = kv_tiles;
+        if (!g.cu_kv && g.causal) {
+          const int qb_last = std::min(max_rows - 1, rt * 128 + 127) / (g.Hq / g.Hkv);
+          t_end = kv_tiles_for(qb_last, g.max_nq, g.max_nkv, 1);
+        }
+        active += (t_end + ch - 1) / ch;
+      }
+      active *= (long long)g.B * g.Hkv;
+      const long long cost = (active + nsm - 1) / nsm * (ch + kDsCtaSetupTiles);
+      if (best < 0 || cost < best) {
+        best = cost;
+        a.ds_chunk = ch;
+      }
+    }
+  }
+  const dim3 ds_grid((kv_tiles + a.ds_chunk - 1) / a.ds_chunk, row_tiles, g.B * g.Hkv);
   // kernels instantiated per padded head dim and input type
   // kernels instantiated per padded head dim, input type and code grid. The INT8 path (the
   // SageAttention (v1) switch) has per-block scales, no Q smoothing and so no DeltaS: the
