@@ -153,7 +153,7 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGE2_OK : SAG
 int prepass_impl(const void *q, const void *k, const void *v, int in_dtype, const int *cu_q,
                  const int *cu_kv, int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q,
                  int total_kv, int D, int causal, float sm_scale, int quant_flags, void *ws,
-                 size_t ws_bytes, void *stream) {
+                 size_t ws_bytes, void *stream, cudaEvent_t q_ready) {
   int rc = check_shapes(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
   if (in_dtype != SAGE2_FP16 && in_dtype != SAGE2_BF16) return SAGE2_EINVAL;
@@ -169,7 +169,7 @@ int prepass_impl(const void *q, const void *k, const void *v, int in_dtype, cons
   if ((rc = check_ws(ws, ws_bytes, L))) return rc;
   if ((rc = check_device())) return rc;
   return cuda_status(
-      launch_prepass(q, k, v, in_dtype, quant_flags, g, L, ws, (cudaStream_t)stream));
+      launch_prepass(q, k, v, in_dtype, quant_flags, g, L, ws, (cudaStream_t)stream, q_ready));
 }
 
 int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, const int *cu_kv,

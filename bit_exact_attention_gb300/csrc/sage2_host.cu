@@ -10,8 +10,9 @@
 // second compute stream, so the first CTAs of one chunk fill the SMs that the last CTAs of the
 // previous one leave idle. Two device slots (inputs, output, workspace) alternate with the
 // chunks; a slot's inputs are refilled as soon as the prepass of its previous chunk has read
-// them, so that copy overlaps the previous chunk's attention. Chunk results are those of the
-// whole problem, bit for bit.
+// them, so that copy overlaps the previous chunk's attention. A chunk's K and V are copied
+// before its Q, and its K/V statistics and codes start while Q is still coming in. Chunk
+// results are those of the whole problem, bit for bit.
 #include <mutex>
 
 #include "sage2_device.cuh"
@@ -58,8 +59,8 @@ struct DevPipe {
   std::mutex mu;
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;  // comp: the odd chunks
-  cudaEvent_t entry = nullptr, in_done[2] = {}, pre_done[2] = {}, comp_done[2] = {},
-              out_done[2] = {};
+  cudaEvent_t entry = nullptr, kv_in[2] = {}, in_done[2] = {}, pre_done[2] = {},
+              comp_done[2] = {}, out_done[2] = {};
 };
 constexpr int kMaxDevices = 64;
 DevPipe g_pipes[kMaxDevices];
@@ -81,7 +82,8 @@ int init_pipe(DevPipe &p) {  // with p.mu held
       cudaEventCreateWithFlags(&p.entry, ef) != cudaSuccess)
     return SAGE2_ECUDA;
   for (int i = 0; i < 2; ++i)
-    if (cudaEventCreateWithFlags(&p.in_done[i], ef) != cudaSuccess ||
+    if (cudaEventCreateWithFlags(&p.kv_in[i], ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.in_done[i], ef) != cudaSuccess ||
         cudaEventCreateWithFlags(&p.pre_done[i], ef) != cudaSuccess ||
         cudaEventCreateWithFlags(&p.comp_done[i], ef) != cudaSuccess ||
         cudaEventCreateWithFlags(&p.out_done[i], ef) != cudaSuccess)
@@ -169,22 +171,26 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
     uint8_t *slot = base + 1024 + sl * p.slot;
     uint8_t *dq = slot, *dk = slot + p.q, *dv = dk + p.kv, *dout = dv + p.kv, *dws = dout + p.o;
     // inputs of chunk c, once the prepass of the slot's previous chunk, c - 2, has read its
-    // inputs (its attention reads only the workspace, so the copy overlaps it)
+    // inputs (its attention reads only the workspace, so the copy overlaps it); K and V first,
+    // so that the chunk's K/V statistics and codes overlap the copy of Q
     if (c >= 2) SAGE2_CK(cudaStreamWaitEvent(pipe->h2d, pipe->pre_done[sl], 0));
-    SAGE2_CK(cudaMemcpy2DAsync(dq, qw, static_cast<const uint8_t *>(q) + c * qw, qpitch, qw,
-                               rows_q, cudaMemcpyHostToDevice, pipe->h2d));
     if (rows_kv) {
       SAGE2_CK(cudaMemcpy2DAsync(dk, kw, static_cast<const uint8_t *>(k) + c * kw, kpitch, kw,
                                  rows_kv, cudaMemcpyHostToDevice, pipe->h2d));
       SAGE2_CK(cudaMemcpy2DAsync(dv, kw, static_cast<const uint8_t *>(v) + c * kw, kpitch, kw,
                                  rows_kv, cudaMemcpyHostToDevice, pipe->h2d));
     }
+    SAGE2_CK(cudaEventRecord(pipe->kv_in[sl], pipe->h2d));
+    SAGE2_CK(cudaMemcpy2DAsync(dq, qw, static_cast<const uint8_t *>(q) + c * qw, qpitch, qw,
+                               rows_q, cudaMemcpyHostToDevice, pipe->h2d));
     SAGE2_CK(cudaEventRecord(pipe->in_done[sl], pipe->h2d));
-    // compute chunk c (its output slot has been copied out)
-    SAGE2_CK(cudaStreamWaitEvent(cs, pipe->in_done[sl], 0));
+    // compute chunk c (its output slot has been copied out); the prepass's Q kernels wait for
+    // the copy of Q
+    SAGE2_CK(cudaStreamWaitEvent(cs, pipe->kv_in[sl], 0));
     if (c >= 2) SAGE2_CK(cudaStreamWaitEvent(cs, pipe->out_done[sl], 0));
     rc = prepass_impl(dq, dk, dv, in_dtype, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq, Nkv, B * Nq,
-                      B * Nkv, D, causal, sm_scale, quant_flags, dws, p.ws, cs);
+                      B * Nkv, D, causal, sm_scale, quant_flags, dws, p.ws, cs,
+                      pipe->in_done[sl]);
     if (rc == SAGE2_OK && cudaEventRecord(pipe->pre_done[sl], cs) != cudaSuccess) rc = SAGE2_ECUDA;
     if (rc == SAGE2_OK)
       rc = attention_impl(dout, out_dtype, quant_flags, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq,

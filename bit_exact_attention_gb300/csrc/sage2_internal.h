@@ -107,11 +107,13 @@ __host__ __device__ inline int kv_tiles_for(int qt, int nq, int nkv, int causal)
 
 // ---------------------------------------------------------------- checked entry points
 // The prepass and attention calls behind the C ABI (argument checks, then the launches);
-// cu_q / cu_kv nullptr for dense problems. Return sage2_status codes.
+// cu_q / cu_kv nullptr for dense problems. Return sage2_status codes. q_ready: when not null,
+// the prepass's Q kernels wait for this event (its K/V statistics and codes do not), so that a
+// caller copying Q in after K and V can overlap the two.
 int prepass_impl(const void *q, const void *k, const void *v, int in_dtype, const int *cu_q,
                  const int *cu_kv, int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q,
                  int total_kv, int D, int causal, float sm_scale, int quant_flags, void *ws,
-                 size_t ws_bytes, void *stream);
+                 size_t ws_bytes, void *stream, cudaEvent_t q_ready = nullptr);
 int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, const int *cu_kv,
                    int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q, int total_kv,
                    int D, int causal, float sm_scale, const void *ws, size_t ws_bytes,
@@ -120,7 +122,7 @@ int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, c
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
                            int quant_flags, const Geometry &g, const Layout &L, void *ws,
-                           cudaStream_t st);
+                           cudaStream_t st, cudaEvent_t q_ready = nullptr);
 
 struct AttnDebug {
   int b, h, qt, kt;        // the single work unit to run (debug launches only)

@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(256) seq_order(const int *cu_kv, int B, int *o
 
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
                            int quant_flags, const Geometry &g, const Layout &L, void *ws,
-                           cudaStream_t st) {
+                           cudaStream_t st, cudaEvent_t q_ready) {
   PrepassArgs a;
   a.q = static_cast<const uint16_t *>(q);
   a.k = static_cast<const uint16_t *>(k);
@@ -927,6 +927,7 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   // kernels instantiated per padded head dim, input type and code grid. The INT8 path (the
   // SageAttention (v1) switch) has per-block scales, no Q smoothing and so no DeltaS: the
   // attention kernel for it reads none.
+  cudaError_t err = cudaSuccess;
   auto run = [&](auto dp_tag, auto bf_tag, auto i8_tag) {
     constexpr int DP = decltype(dp_tag)::value;
     constexpr bool BF = decltype(bf_tag)::value;
@@ -938,6 +939,7 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
       kv_stats_final<8><<<dim3(g.B * g.Hkv, g.Dp / 8), kFinalThreads, 0, st>>>(a);
     k_quant<DP, BF, I8><<<kv_grid, 256, 0, st>>>(a);
     v_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
+    if (q_ready && (err = cudaStreamWaitEvent(st, q_ready, 0)) != cudaSuccess) return;
     q_quant<DP, BF, I8><<<q_grid, 256, 0, st>>>(a);
     if (I8) return;
     constexpr int kSmem = DsPlan<DP>::kBytes;
@@ -947,7 +949,7 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
       attr_err = cudaFuncSetAttribute(delta_s_tc<DP, BF>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     });
-    if (attr_err != cudaSuccess) return;
+    if ((err = attr_err) != cudaSuccess) return;
     delta_s_tc<DP, BF><<<ds_grid, kDsThreads, kSmem, st>>>(a);
   };
   auto run_dp = [&](auto i8_tag) {
@@ -963,7 +965,8 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   };
   if (int8) run_dp(std::true_type());
   else run_dp(std::false_type());
-  return cudaGetLastError();
+  const cudaError_t last = cudaGetLastError();
+  return err != cudaSuccess ? err : last;
 }
 
 }  // namespace sage2
