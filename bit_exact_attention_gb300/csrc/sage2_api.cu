@@ -175,12 +175,13 @@ int prepass_impl(const void *q, const void *k, const void *v, int in_dtype, cons
 int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, const int *cu_kv,
                    int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q, int total_kv,
                    int D, int causal, float sm_scale, const void *ws, size_t ws_bytes,
-                   void *stream) {
+                   void *stream, int hq0, int hq_n) {
   int rc = check_shapes(B, Hq, Hkv, max_nq, max_nkv, D, total_q, total_kv, causal);
   if (rc) return rc;
   if (!valid_quant_flags(quant_flags)) return SAGE2_EINVAL;
   if (out_dtype != SAGE2_FP16 && out_dtype != SAGE2_BF16 && out_dtype != SAGE2_FP32)
     return SAGE2_EINVAL;
+  if (hq0 < 0 || hq_n < 0 || hq0 + hq_n > Hq || (hq_n == 0 && hq0 >= Hq)) return SAGE2_EINVAL;
   if (total_q > 0 && (!out || !aligned16(out))) return SAGE2_EINVAL;
   Geometry g;
   Layout L;
@@ -191,7 +192,7 @@ int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, c
   if ((rc = check_device())) return rc;
   if (total_q == 0 || max_nq == 0) return SAGE2_OK;
   return cuda_status(launch_attention(out, out_dtype, g, L, ws, (cudaStream_t)stream, nullptr,
-                                      (quant_flags & SAGE2_QUANT_SAGE1) != 0));
+                                      (quant_flags & SAGE2_QUANT_SAGE1) != 0, hq0, hq_n));
 }
 
 }  // namespace sage2

@@ -102,6 +102,7 @@ struct AttnArgs {
   int out_dtype;
   int *status;
   const int *seq_order;  // varlen: the sequence each z index takes (two-tile kernel)
+  int hq0, hq_n;         // the q heads [hq0, hq0 + hq_n) of this launch
   AttnDebug dbg;
 };
 
@@ -310,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ob = a.seq_order[blockIdx.z];
       if (ob >= 0 && ob < g.B) b = ob;
     }
-    hq = (int)blockIdx.x % g.Hq;
-    const int ntiles = (int)gridDim.x / g.Hq, tidx = (int)blockIdx.x / g.Hq;
+    hq = a.hq0 + (int)blockIdx.x % a.hq_n;
+    const int ntiles = (int)gridDim.x / a.hq_n, tidx = (int)blockIdx.x / a.hq_n;
     qt = g.causal ? ntiles - 1 - tidx : tidx;
   }
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
@@ -830,8 +831,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ob >= 0 && ob < g.B) b = ob;  // (a workspace of another prepass keeps the batch order)
   }
   if (DBG) b = a.dbg.b;
-  const int npairs = (int)gridDim.x / g.Hq, pidx = (int)blockIdx.x / g.Hq;
-  const int hq = DBG ? a.dbg.h : (int)blockIdx.x % g.Hq;
+  const int npairs = (int)gridDim.x / a.hq_n, pidx = (int)blockIdx.x / a.hq_n;
+  const int hq = DBG ? a.dbg.h : a.hq0 + (int)blockIdx.x % a.hq_n;
   const int pair = DBG ? a.dbg.qt / 2 : (g.causal ? npairs - 1 - pidx : pidx);
   const Seq s = seq_info(g.cu_q, g.cu_kv, b, g.max_nq, g.max_nkv);
   if (format != kFormatInt4) {
@@ -1280,7 +1281,8 @@ bool use_pp() {
 }  // namespace
 
 cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const Layout &L,
-                             const void *ws, cudaStream_t st, const AttnDebug *dbg, bool int8_qk) {
+                             const void *ws, cudaStream_t st, const AttnDebug *dbg, bool int8_qk,
+                             int hq0, int hq_n) {
   if (int8_qk != (L.code_bytes == 2)) return cudaErrorInvalidValue;
   const WsPtrs w = ws_ptrs(const_cast<void *>(ws), L);
   AttnArgs a;
@@ -1296,6 +1298,9 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
   a.status = w.status;
   a.seq_order = w.status + kSeqOrderWord;
   a.dbg = dbg ? *dbg : AttnDebug{0, 0, 0, 0, nullptr, nullptr, nullptr, 0};
+  if (hq0 < 0 || hq_n < 0 || hq0 + hq_n > g.Hq) return cudaErrorInvalidValue;
+  a.hq0 = hq0;
+  a.hq_n = hq_n > 0 ? hq_n : g.Hq - hq0;
   const CUtensorMapSwizzle qk_sw =
       g.Dp == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap mk, mv;
@@ -1311,7 +1316,7 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
     CUtensorMap mq;
     if (!make_map(&mq, w.qcode, g.Dp, (uint64_t)g.Hq * L.Tq, g.Dp, 128, qk_sw))
       return cudaErrorInvalidValue;
-    const dim3 grid2(g.Hq * ((nqt + 1) / 2), 1, g.B);
+    const dim3 grid2(a.hq_n * ((nqt + 1) / 2), 1, g.B);
     // K and V stages: 3 each at D = 128; 8 each at D = 64 (no P~ buffers in shared memory there;
     // 8 measured 1.5 % faster than 6 on the video DiT shape, 10 no better)
     if (dbg) {
@@ -1321,7 +1326,7 @@ cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const 
     if (g.Dp == 128) return launch_pp<128, 3, false>(mq, mk, mv, a, grid2, st);
     return launch_pp<64, 8, false>(mq, mk, mv, a, grid2, st);
   }
-  const dim3 grid = dbg ? dim3(1) : dim3(g.Hq * nqt, 1, g.B);
+  const dim3 grid = dbg ? dim3(1) : dim3(a.hq_n * nqt, 1, g.B);
   // pipeline depth: as many K/V stages as fit (a stage of fp16 K codes is twice as large)
   if (int8_qk) {
     if (dbg) {

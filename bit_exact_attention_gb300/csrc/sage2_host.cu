@@ -59,8 +59,9 @@ struct DevPipe {
   std::mutex mu;
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;  // comp: the odd chunks
+  cudaStream_t tail = nullptr;  // the second half of the last chunk's attention
   cudaEvent_t entry = nullptr, kv_in[2] = {}, in_done[2] = {}, pre_done[2] = {},
-              comp_done[2] = {}, out_done[2] = {};
+              comp_done[2] = {}, out_done[2] = {}, half_done = nullptr;
 };
 constexpr int kMaxDevices = 64;
 DevPipe g_pipes[kMaxDevices];
@@ -79,7 +80,9 @@ int init_pipe(DevPipe &p) {  // with p.mu held
   if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&p.entry, ef) != cudaSuccess)
+      cudaStreamCreateWithFlags(&p.tail, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p.entry, ef) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p.half_done, ef) != cudaSuccess)
     return SAGE2_ECUDA;
   for (int i = 0; i < 2; ++i)
     if (cudaEventCreateWithFlags(&p.kv_in[i], ef) != cudaSuccess ||
@@ -148,9 +151,10 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
   // On an error after work was queued, the given stream still waits for everything queued on
   // the copy and compute streams (a caller that synchronizes it may then reuse its buffers).
   auto join = [&]() {
-    cudaEvent_t done[3] = {pipe->in_done[0], pipe->comp_done[0], pipe->out_done[0]};
-    const cudaStream_t side[3] = {pipe->h2d, pipe->comp, pipe->d2h};
-    for (int i = 0; i < 3; ++i)
+    cudaEvent_t done[4] = {pipe->in_done[0], pipe->comp_done[0], pipe->out_done[0],
+                           pipe->half_done};
+    const cudaStream_t side[4] = {pipe->h2d, pipe->comp, pipe->d2h, pipe->tail};
+    for (int i = 0; i < 4; ++i)
       if (cudaEventRecord(done[i], side[i]) == cudaSuccess) cudaStreamWaitEvent(s0, done[i], 0);
   };
 #define SAGE2_CK(x)              \
@@ -165,6 +169,7 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
   SAGE2_CK(cudaStreamWaitEvent(pipe->h2d, pipe->entry, 0));
   SAGE2_CK(cudaStreamWaitEvent(pipe->d2h, pipe->entry, 0));
   SAGE2_CK(cudaStreamWaitEvent(pipe->comp, pipe->entry, 0));
+  SAGE2_CK(cudaStreamWaitEvent(pipe->tail, pipe->entry, 0));
   for (int c = 0; c < p.chunks; ++c) {
     const int sl = c & 1;
     const cudaStream_t cs = sl ? pipe->comp : s0;  // the slot's compute stream
@@ -192,19 +197,41 @@ extern "C" int sage2_attn_fwd_host(const void *q, const void *k, const void *v, 
                       B * Nkv, D, causal, sm_scale, quant_flags, dws, p.ws, cs,
                       pipe->in_done[sl]);
     if (rc == SAGE2_OK && cudaEventRecord(pipe->pre_done[sl], cs) != cudaSuccess) rc = SAGE2_ECUDA;
+    // The last chunk's output copy has nothing left to overlap: its attention runs as two
+    // launches over halves of its q heads (the second on its own stream, so its CTAs fill the
+    // first one's tail), and the first half is copied out while the second computes.
+    const int h1 = (c == p.chunks - 1) ? p.hq_c / 2 : 0;
     if (rc == SAGE2_OK)
       rc = attention_impl(dout, out_dtype, quant_flags, nullptr, nullptr, B, p.hq_c, p.hk_c, Nq,
-                          Nkv, B * Nq, B * Nkv, D, causal, sm_scale, dws, p.ws, cs);
+                          Nkv, B * Nq, B * Nkv, D, causal, sm_scale, dws, p.ws, cs, 0, h1);
+    if (rc == SAGE2_OK && h1 > 0) {
+      if (cudaEventRecord(pipe->half_done, cs) != cudaSuccess ||
+          cudaStreamWaitEvent(pipe->tail, pipe->pre_done[sl], 0) != cudaSuccess)
+        rc = SAGE2_ECUDA;
+      else
+        rc = attention_impl(dout, out_dtype, quant_flags, nullptr, nullptr, B, p.hq_c, p.hk_c,
+                            Nq, Nkv, B * Nq, B * Nkv, D, causal, sm_scale, dws, p.ws, pipe->tail,
+                            h1, p.hq_c - h1);
+    }
     if (rc) {
       join();
       return rc;
     }
-    merge_status<<<1, 1, 0, cs>>>(reinterpret_cast<const int *>(base1k(dws)), status_total);
+    const cudaStream_t cs_end = h1 > 0 ? pipe->tail : cs;  // after both halves
+    if (h1 > 0) SAGE2_CK(cudaStreamWaitEvent(pipe->tail, pipe->half_done, 0));
+    merge_status<<<1, 1, 0, cs_end>>>(reinterpret_cast<const int *>(base1k(dws)), status_total);
     SAGE2_CK(cudaGetLastError());
-    SAGE2_CK(cudaEventRecord(pipe->comp_done[sl], cs));
-    // output of chunk c
+    SAGE2_CK(cudaEventRecord(pipe->comp_done[sl], cs_end));
+    // output of chunk c (the first half of the last chunk's heads as soon as it is done)
+    uint8_t *hout = static_cast<uint8_t *>(out) + c * ow;
+    const size_t hw = (size_t)h1 * D * ob;  // bytes of a row's first h1 heads
+    if (h1 > 0) {
+      SAGE2_CK(cudaStreamWaitEvent(pipe->d2h, pipe->half_done, 0));
+      SAGE2_CK(cudaMemcpy2DAsync(hout, opitch, dout, ow, hw, rows_q, cudaMemcpyDeviceToHost,
+                                 pipe->d2h));
+    }
     SAGE2_CK(cudaStreamWaitEvent(pipe->d2h, pipe->comp_done[sl], 0));
-    SAGE2_CK(cudaMemcpy2DAsync(static_cast<uint8_t *>(out) + c * ow, opitch, dout, ow, ow, rows_q,
+    SAGE2_CK(cudaMemcpy2DAsync(hout + hw, opitch, dout + hw, ow, ow - hw, rows_q,
                                cudaMemcpyDeviceToHost, pipe->d2h));
     SAGE2_CK(cudaEventRecord(pipe->out_done[sl], pipe->d2h));
   }

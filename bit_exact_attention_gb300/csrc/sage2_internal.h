@@ -114,10 +114,12 @@ int prepass_impl(const void *q, const void *k, const void *v, int in_dtype, cons
                  const int *cu_kv, int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q,
                  int total_kv, int D, int causal, float sm_scale, int quant_flags, void *ws,
                  size_t ws_bytes, void *stream, cudaEvent_t q_ready = nullptr);
+// hq0, hq_n: attention for the q heads [hq0, hq0 + hq_n) only (hq_n = 0: through the last);
+// the other heads' output rows are left as they are.
 int attention_impl(void *out, int out_dtype, int quant_flags, const int *cu_q, const int *cu_kv,
                    int B, int Hq, int Hkv, int max_nq, int max_nkv, int total_q, int total_kv,
                    int D, int causal, float sm_scale, const void *ws, size_t ws_bytes,
-                   void *stream);
+                   void *stream, int hq0 = 0, int hq_n = 0);
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
@@ -132,9 +134,10 @@ struct AttnDebug {
   int skip_loads;          // producer issues nothing: every wait must time out
 };
 // int8_qk: the INT8-grid variant (Q K^T on fp16 codes); the workspace must come from a prepass
-// with SAGE2_QUANT_SAGE1, and the other way round (checked on the device).
+// with SAGE2_QUANT_SAGE1, and the other way round (checked on the device). hq0, hq_n: only the
+// q heads [hq0, hq0 + hq_n) (hq_n = 0: through the last head).
 cudaError_t launch_attention(void *out, int out_dtype, const Geometry &g, const Layout &L,
                              const void *ws, cudaStream_t st, const AttnDebug *dbg,
-                             bool int8_qk = false);
+                             bool int8_qk = false, int hq0 = 0, int hq_n = 0);
 
 }  // namespace sage2
