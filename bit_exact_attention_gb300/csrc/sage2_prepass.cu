@@ -861,6 +861,34 @@ __global__ void __launch_bounds__(256) seq_order(const int *cu_kv, int B, int *o
   }
 }
 
+// Two side streams per device on which the prepass runs the kernels that do not depend on the
+// K/V chain before them (the Q codes; the V codes next to the K codes), forked from and joined
+// back into the caller's stream with events. One mutex per device makes each call's record /
+// wait sequence whole, so concurrent callers cannot wait on one another's events.
+struct SideStreams {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t s[2] = {nullptr, nullptr};
+  cudaEvent_t fork = nullptr, kv_done = nullptr, q_done = nullptr, v_done = nullptr;
+};
+constexpr int kMaxDevices = 64;
+SideStreams g_side[kMaxDevices];
+
+cudaError_t init_side(SideStreams &p) {  // with p.mu held
+  if (p.ready) return cudaSuccess;
+  const unsigned ef = cudaEventDisableTiming;
+  cudaError_t e;
+  for (int i = 0; i < 2; ++i)
+    if ((e = cudaStreamCreateWithFlags(&p.s[i], cudaStreamNonBlocking)) != cudaSuccess) return e;
+  if ((e = cudaEventCreateWithFlags(&p.fork, ef)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&p.kv_done, ef)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&p.q_done, ef)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&p.v_done, ef)) != cudaSuccess)
+    return e;
+  p.ready = true;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_dtype,
@@ -894,10 +922,9 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   // DeltaS: 128-row tiles of (Q block, q head) pairs, a.ds_chunk key tiles per CTA
   const int max_rows = (g.Hq / g.Hkv) * q_tiles;
   const int row_tiles = (max_rows + 127) / 128;
-  int nsm = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    nsm = 0;
+  int nsm = 0, dev = -1;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) nsm = 0;
   a.ds_chunk = kDsChunkMax;
   if (nsm > 0) {
     // CTAs with work per chunk size: a dense call's row tile rt visits the key tiles of its last
@@ -927,20 +954,38 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   // kernels instantiated per padded head dim, input type and code grid. The INT8 path (the
   // SageAttention (v1) switch) has per-block scales, no Q smoothing and so no DeltaS: the
   // attention kernel for it reads none.
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStreams &side = g_side[dev];
+  std::lock_guard<std::mutex> lock(side.mu);
+  if ((e = init_side(side)) != cudaSuccess) return e;
   cudaError_t err = cudaSuccess;
+  // Q codes on side stream 0 from the start (after the status words; once q_ready has fired,
+  // when given), V codes on side stream 1 once the statistics are final, K codes and then DeltaS
+  // on the caller's stream, which waits for both side streams before DeltaS.
   auto run = [&](auto dp_tag, auto bf_tag, auto i8_tag) {
     constexpr int DP = decltype(dp_tag)::value;
     constexpr bool BF = decltype(bf_tag)::value;
     constexpr bool I8 = decltype(i8_tag)::value;
+    if ((err = cudaEventRecord(side.fork, st)) != cudaSuccess ||
+        (err = cudaStreamWaitEvent(side.s[0], side.fork, 0)) != cudaSuccess ||
+        (q_ready && (err = cudaStreamWaitEvent(side.s[0], q_ready, 0)) != cudaSuccess))
+      return;
+    q_quant<DP, BF, I8><<<q_grid, 256, 0, side.s[0]>>>(a);
+    if ((err = cudaEventRecord(side.q_done, side.s[0])) != cudaSuccess) return;
     kv_stats_partial<BF><<<stat_grid, kStatThreads, 0, st>>>(a);
     if (g.B * g.Hkv * (g.Dp / 32) >= 64)
       kv_stats_final<32><<<dim3(g.B * g.Hkv, g.Dp / 32), kFinalThreads, 0, st>>>(a);
     else
       kv_stats_final<8><<<dim3(g.B * g.Hkv, g.Dp / 8), kFinalThreads, 0, st>>>(a);
+    if ((err = cudaEventRecord(side.kv_done, st)) != cudaSuccess ||
+        (err = cudaStreamWaitEvent(side.s[1], side.kv_done, 0)) != cudaSuccess)
+      return;
+    v_quant<DP, BF><<<kv_grid, 256, 0, side.s[1]>>>(a);
+    if ((err = cudaEventRecord(side.v_done, side.s[1])) != cudaSuccess) return;
     k_quant<DP, BF, I8><<<kv_grid, 256, 0, st>>>(a);
-    v_quant<DP, BF><<<kv_grid, 256, 0, st>>>(a);
-    if (q_ready && (err = cudaStreamWaitEvent(st, q_ready, 0)) != cudaSuccess) return;
-    q_quant<DP, BF, I8><<<q_grid, 256, 0, st>>>(a);
+    if ((err = cudaStreamWaitEvent(st, side.q_done, 0)) != cudaSuccess ||
+        (err = cudaStreamWaitEvent(st, side.v_done, 0)) != cudaSuccess)
+      return;
     if (I8) return;
     constexpr int kSmem = DsPlan<DP>::kBytes;
     static std::once_flag once;
