@@ -98,7 +98,12 @@ int sage2_attn_fwd_varlen(const void *q, const void *k, const void *v, void *out
  * apart. sage2_prepass*: smoothing and quantization only (K/V statistics, Q/K INT4 codes
  * and scales, V e4m3 codes transposed, DeltaS), written into the workspace.
  * sage2_attention*: the fused attention kernel only, reading a workspace that a prepass
- * call with the same arguments filled. */
+ * call with the same arguments filled.
+ * Every prepass (these and the one inside the full forwards) runs its Q codes and V codes on
+ * two library-owned streams, forked from `stream` and joined back into it with events before
+ * the call's last kernel, so the call stays ordered on `stream` as a whole. The first prepass
+ * on a device creates those streams and events (kept until the process exits): make it before
+ * any stream capture. */
 int sage2_prepass(const void *q, const void *k, const void *v, int in_dtype, int B, int Hq,
                   int Hkv, int Nq, int Nkv, int D, int causal, float sm_scale, void *workspace,
                   size_t workspace_bytes, void *stream);
