@@ -960,8 +960,9 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
   if ((e = init_side(side)) != cudaSuccess) return e;
   cudaError_t err = cudaSuccess;
   // Q codes on side stream 0 from the start (after the status words; once q_ready has fired,
-  // when given), V codes on side stream 1 once the statistics are final, K codes and then DeltaS
-  // on the caller's stream, which waits for both side streams before DeltaS.
+  // when given); the statistics on the caller's stream, then the V and K codes on side stream 1
+  // while DeltaS (which needs the K means and the Q block means, not the K codes) runs on the
+  // caller's stream; that stream finally waits for side stream 1.
   auto run = [&](auto dp_tag, auto bf_tag, auto i8_tag) {
     constexpr int DP = decltype(dp_tag)::value;
     constexpr bool BF = decltype(bf_tag)::value;
@@ -981,12 +982,14 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
         (err = cudaStreamWaitEvent(side.s[1], side.kv_done, 0)) != cudaSuccess)
       return;
     v_quant<DP, BF><<<kv_grid, 256, 0, side.s[1]>>>(a);
-    if ((err = cudaEventRecord(side.v_done, side.s[1])) != cudaSuccess) return;
-    k_quant<DP, BF, I8><<<kv_grid, 256, 0, st>>>(a);
-    if ((err = cudaStreamWaitEvent(st, side.q_done, 0)) != cudaSuccess ||
-        (err = cudaStreamWaitEvent(st, side.v_done, 0)) != cudaSuccess)
+    k_quant<DP, BF, I8><<<kv_grid, 256, 0, side.s[1]>>>(a);
+    if ((err = cudaEventRecord(side.v_done, side.s[1])) != cudaSuccess ||
+        (err = cudaStreamWaitEvent(st, side.q_done, 0)) != cudaSuccess)
       return;
-    if (I8) return;
+    if (I8) {
+      err = cudaStreamWaitEvent(st, side.v_done, 0);
+      return;
+    }
     constexpr int kSmem = DsPlan<DP>::kBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -994,8 +997,12 @@ cudaError_t launch_prepass(const void *q, const void *k, const void *v, int in_d
       attr_err = cudaFuncSetAttribute(delta_s_tc<DP, BF>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     });
-    if ((err = attr_err) != cudaSuccess) return;
+    if ((err = attr_err) != cudaSuccess) {
+      cudaStreamWaitEvent(st, side.v_done, 0);  // still join the side stream
+      return;
+    }
     delta_s_tc<DP, BF><<<ds_grid, kDsThreads, kSmem, st>>>(a);
+    err = cudaStreamWaitEvent(st, side.v_done, 0);
   };
   auto run_dp = [&](auto i8_tag) {
     using T128 = std::integral_constant<int, 128>;
