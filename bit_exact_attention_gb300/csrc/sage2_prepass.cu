@@ -861,9 +861,9 @@ __global__ void __launch_bounds__(256) seq_order(const int *cu_kv, int B, int *o
   }
 }
 
-// Two side streams per device on which the prepass runs the kernels that do not depend on the
-// K/V chain before them (the Q codes; the V codes next to the K codes), forked from and joined
-// back into the caller's stream with events. One mutex per device makes each call's record /
+// Two side streams per device on which the prepass runs the kernels that do not wait for the
+// launches before them on the caller's stream (the Q codes from the start; the V and K codes
+// next to DeltaS), forked from and joined back into the caller's stream with events. One mutex per device makes each call's record /
 // wait sequence whole, so concurrent callers cannot wait on one another's events.
 struct SideStreams {
   std::mutex mu;
