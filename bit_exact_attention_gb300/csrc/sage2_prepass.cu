@@ -367,6 +367,20 @@ __global__ void __launch_bounds__(256) v_quant(PrepassArgs a) {
   }
 }
 
+// fl32(sum / n) of an exact FP64 sum over n rows. A whole block (n = 128) divides by a power of
+// two, so the quotient is exact and fl32(sum / 128) = fl32(sum) * 2^-7 whenever that is a normal
+// float; this skips the FP64 division, which GB300's few FP64 units made the bottleneck of the Q
+// codes kernel (one per channel of every block). Other n, and results outside the normal range,
+// take the division.
+__device__ __forceinline__ float block_mean(double sum, int n) {
+  if (n == kBQ) {
+    const float f = __double2float_rn(sum);
+    const float af = fabsf(f);
+    if (af == 0.f || (af >= 0x1p-119f && af <= 0x1p127f)) return __fmul_rn(f, 1.f / kBQ);
+  }
+  return __double2float_rn(sum / (double)n);
+}
+
 // ------------------------------------------------------------------ 4. Q codes
 // grid (ceil(max_nq / 128), Hq, B), block 256. The block's 128 x D0 input values are staged in
 // shared memory with asynchronous 16-byte copies (few registers, so many CTAs per SM keep enough
@@ -428,7 +442,7 @@ __global__ void __launch_bounds__(256) q_quant(PrepassArgs a) {
 #pragma unroll
     for (int p = 1; p < kParts; ++p) sum += colsum[p][d];
     const bool smooth = !(a.flags & SAGE2_QUANT_NO_SMOOTH_Q);
-    const float m = (smooth && nvalid > 0 && d < g.D0) ? (float)(sum / (double)nvalid) : 0.f;
+    const float m = (smooth && nvalid > 0 && d < g.D0) ? block_mean(sum, nvalid) : 0.f;
     qbar[d] = m;
     a.w.qmean[((size_t)h * a.L.nqblk + s.qpad0 / kBQ + qb) * DP + d] = m;
   }
