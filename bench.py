@@ -484,7 +484,9 @@ def run_ours(args, rank, world, local):
     ms_per_step = total_s * 1e3 / args.steps
     att_mean = statistics.mean(att_ms)
     pre_mean = statistics.mean(pre_ms)
-    kernels_per_step = 6 if sage1 else 7  # prepass: 6 kernels (5 without DeltaS); attention: 1
+    # prepass: the varlen sequence order, the K/V statistics (2), the K, V and Q codes and (not
+    # on the v1 path) DeltaS; attention: 1
+    kernels_per_step = 7 if sage1 else 8
 
     # end to end through the public API: pinned host inputs in, host output back
     e2e = None
