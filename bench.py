@@ -265,7 +265,10 @@ def run_oracle_sample(w: W.Workload, x: dict, units, quant="sage2"):
 
 
 def sample_size(w: W.Workload) -> int:
-    return 12 if max(w.nkv) >= 16384 else 32
+    """(sequence, head, Q block) units of the CPU oracle's sample: about 10 s of work on 16 host
+    cores for the long-context workloads (each unit there sees up to 32k keys), more units of the
+    shorter ones (at most all of them)."""
+    return 512 if max(w.nkv) >= 16384 else 2048
 
 
 # ------------------------------------------------------------------ per-workload figures
