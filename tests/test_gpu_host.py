@@ -23,6 +23,9 @@ CASES = [
     (W.scaled(W.PREFILL, (384, 384), (384, 384), hq=4, hkv=2, name="prefill_d"), (1, 2)),
     (W.scaled(W.GQA_LONG, (1000,), (1000,), hq=8, hkv=4, name="gqa_d"), (1, 2, 4)),
     (W.scaled(W.VIDEO_DIT, (333, 333), (333, 333), hq=3, hkv=3, name="dit_d"), (1, 3)),
+    # causal with Nq != Nkv (bottom-right aligned), both ways, GQA groups of 3
+    (W.scaled(W.GQA_LONG, (300,), (700,), hq=6, hkv=2, name="gqa_q_lt_kv"), (1, 2)),
+    (W.scaled(W.GQA_LONG, (650,), (260,), hq=6, hkv=2, name="gqa_q_gt_kv"), (1, 2)),
 ]
 
 
